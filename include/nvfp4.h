@@ -1,0 +1,221 @@
+/*
+ * nvfp4.h - C ABI of libnvfp4.so: the NVFP4 block-scaled linear layer of a
+ * 4-bit LLM serving engine, on one NVIDIA GB300 (sm_103a).
+ *
+ * The format. "NVFP4 is 4-bit e2m1 with per-16 FP8 scales" (Serving
+ * Qwen3.8-27B in 4-bit with a masked speculative decoding head, "What the
+ * artifact is"); the FP8 scale is E4M3, four exponent and three mantissa bits
+ * (What 350+ Experiments Taught Us About Serving Qwen 3.6 35B-A3B, section 3).
+ * A tensor T[rows][K] is stored as
+ *   codes   uint8 [rows][K/2]   element 2j in the low nibble of byte j,
+ *                               element 2j+1 in the high nibble;
+ *   scales  uint8 [rows][K/16]  one E4M3 block scale per 16 elements along K
+ *                               (row-major; or the MMA layout, see below);
+ *   s_t     fp32                 one tensor scale (device memory).
+ * and decodes to  x_hat[r][k] = e2m1(code) * e4m3(scale[r][k/16]) * s_t.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers unless stated otherwise; the caller owns
+ *    every buffer. The library allocates nothing.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream); nothing
+ *    synchronises the host.
+ *  - Return value: NVFP4_OK (0) or a negative NVFP4_ERR_*; arguments are
+ *    validated on the host before anything is launched, so an error return
+ *    means nothing was enqueued (except NVFP4_ERR_CUDA, raised by a failed
+ *    launch). The library never aborts and prints nothing.
+ *  - bf16 means IEEE-style bfloat16 (uint16 storage), row-major.
+ *  - Base pointers of codes, activations and outputs must be 16-byte aligned.
+ *  - No CPU fallback exists: every call runs CUDA kernels on the current
+ *    device.
+ */
+#ifndef NVFP4_H_
+#define NVFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* nvfp4_stream_t;   /* == cudaStream_t */
+
+/* ---- status codes ------------------------------------------------------ */
+#define NVFP4_OK                     0
+#define NVFP4_ERR_INVALID_ARG       -1   /* null pointer, negative size, bad enum */
+#define NVFP4_ERR_UNSUPPORTED_SHAPE -2   /* a size is not a multiple of the op's granule */
+#define NVFP4_ERR_MISALIGNED        -3   /* a pointer that must be 16-byte aligned is not */
+#define NVFP4_ERR_CUDA              -4   /* a CUDA runtime / driver call failed */
+#define NVFP4_ERR_WORKSPACE         -5   /* workspace missing or too small */
+#define NVFP4_ERR_TIMEOUT           -6   /* a bounded on-device wait gave up (device status word) */
+
+/* ---- enums --------------------------------------------------------------- */
+#define NVFP4_DTYPE_F32   0
+#define NVFP4_DTYPE_BF16  1
+
+#define NVFP4_ST_COMPUTE  0   /* s_t = amax(|x|) / 2688 (1 if all zero), written to *s_t */
+#define NVFP4_ST_GIVEN    1   /* s_t read from *s_t (must be finite and > 0) */
+
+/* Scale layouts.
+ * ROWMAJOR: scales[r][j] at r*(K/16) + j.
+ * MMA: the layout the block-scaled tensor-core MMA consumes. Rows are padded
+ *   to a multiple of 128 and the K/16 scale columns to a multiple of 4; the
+ *   padded matrix is cut into 128x4 tiles of 512 bytes, tile (rt, ct) at byte
+ *   (rt * (Kp/64) + ct) * 512, and inside a tile row r, column c sits at
+ *   (r % 32) * 16 + (r / 32) * 4 + c. Padding bytes are zero. */
+#define NVFP4_SCALES_ROWMAJOR 0
+#define NVFP4_SCALES_MMA      1
+
+/* An NVFP4 tensor (or a stack of `batch` equally shaped ones, e.g. the
+ * experts of a MoE layer). Matrix b starts at codes + b*rows*K/2, at
+ * scales + b*nvfp4_scales_bytes(rows, K, scale_layout), and its tensor scale
+ * is s_t[b] (device memory). */
+typedef struct nvfp4_tensor {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* s_t;
+  int64_t rows;
+  int64_t K;
+  int32_t batch;
+  int32_t scale_layout;
+} nvfp4_tensor_t;
+
+/* Operation ids for nvfp4_workspace_size. */
+#define NVFP4_OP_QUANTIZE        0
+#define NVFP4_OP_GEMM_W4A16      1
+#define NVFP4_OP_GEMM_W4A4       2
+#define NVFP4_OP_GROUPED_GEMM    3
+#define NVFP4_OP_GATHER_ARGMAX   4
+
+/* ---- entry points ----------------------------------------------------------- */
+
+/* Quantise x[rows][K] (fp32 or bf16) to NVFP4.
+ * The per-16 block scale is amax(|block|)/6 rounded to E4M3 (nearest, ties
+ * to even, saturating at 448), taken relative to the tensor scale; each
+ * element is x / (e4m3(scale) * s_t) rounded to e2m1 (nearest, ties to the
+ * even code, saturating at 6; the sign of a negative element is kept even
+ * when its magnitude rounds to zero; a zero scale gives zero codes). All
+ * decisions are fp32 with IEEE division. The format is the pages' (see the
+ * top of this file); the rounding rules are readings of it.
+ *   x          device, rows*K elements of x_dtype, 16-byte aligned
+ *   codes      device out, rows*K/2 bytes, 16-byte aligned
+ *   scales     device out, nvfp4_scales_bytes(rows, K, scale_layout) bytes
+ *   s_t        device fp32: written (COMPUTE) or read (GIVEN)
+ *   workspace  device, >= nvfp4_workspace_size(NVFP4_OP_QUANTIZE, ...) bytes
+ *              (COMPUTE only; may be NULL for GIVEN); contents are scratch.
+ * K must be a multiple of 16. rows == 0 is a no-op (COMPUTE writes s_t = 1). */
+int nvfp4_quantize(const void* x, int x_dtype, int64_t rows, int64_t K,
+                   uint8_t* codes, uint8_t* scales, float* s_t, int s_t_mode,
+                   int scale_layout, void* workspace, size_t workspace_bytes,
+                   nvfp4_stream_t stream);
+
+/* Re-lay row-major block scales into the MMA layout (a one-time weight
+ * prepack; activations can be quantised straight into the MMA layout).
+ *   src  device, batch*rows*(K/16) bytes, row-major
+ *   dst  device, batch*nvfp4_scales_bytes(rows, K, NVFP4_SCALES_MMA) bytes */
+int nvfp4_prepack_scales(const uint8_t* src, int64_t batch, int64_t rows, int64_t K,
+                         uint8_t* dst, nvfp4_stream_t stream);
+
+/* W4A16 linear (decode): Y[m][n] = bf16( sum_k X[m][k] * W_hat[n][k] ) with
+ * fp32 accumulation - "four-bit weights and 16-bit activations" (What 350+
+ * Experiments..., section 1; Qwen3.8-27B benchmark, "Serving configuration
+ * measured").
+ *   X  device bf16 [M][K];  W  NVFP4 [N][K], batch 1, ROWMAJOR scales;
+ *   Y  device bf16 [M][N].
+ *   workspace  >= nvfp4_workspace_size(NVFP4_OP_GEMM_W4A16, M, N, K) bytes:
+ *              the activations converted to f16 (each token times a power of
+ *              two that keeps it in f16 range, exact) in MMA fragment order.
+ * K must be a multiple of 128. Any M >= 1 (tuned for M <= 32). */
+int nvfp4_gemm_w4a16(const void* X, int64_t M, nvfp4_tensor_t W, void* Y,
+                     void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* W4A4 linear (prefill): Y[m][n] = bf16( s_tA * s_tW * sum_k a[m][k] * w[n][k] )
+ * where a, w are the e2m1*e4m3 products, multiplied and accumulated (fp32) by
+ * the block-scaled FP4 tensor cores - "Blackwell-native NVFP4 W4A4 execution"
+ * (52.6% More Tokens, 1.53x Less GPU Time: Production Inference with Minima
+ * and Rafay).
+ *   A  NVFP4 [M][K] (typically from nvfp4_quantize, COMPUTE);
+ *   W  NVFP4 [N][K]; both batch 1. MMA-layout scales are used in place;
+ *      ROWMAJOR scales are re-laid into the workspace first.
+ *   Y  device bf16 [M][N].
+ *   workspace >= nvfp4_workspace_size(NVFP4_OP_GEMM_W4A4, M, N, K) when an
+ *      operand has ROWMAJOR scales; unused (may be NULL) otherwise.
+ * K must be a multiple of 64 and N a multiple of 8; M >= 1 arbitrary. */
+int nvfp4_gemm_w4a4(nvfp4_tensor_t A, nvfp4_tensor_t W, void* Y,
+                    void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* Top-k routing of a MoE layer: p = softmax(logits[t]) (fp32), the k experts
+ * with the largest p (ties to the lower expert id), weights = those p (not
+ * renormalised). ids int32 [T][topk], weights fp32 [T][topk], in descending
+ * p order. E <= 1024, topk <= 32. */
+int nvfp4_moe_route(const float* logits, int64_t T, int E, int topk,
+                    int32_t* ids, float* weights, nvfp4_stream_t stream);
+
+/* Routed-expert MoE layer, W4A16 (What 350+ Experiments..., sections 1 and 7:
+ * NVFP4 mixture-of-experts operations):
+ *   for each token t and slot j with e = topk_ids[t][j]:
+ *     [g; u] = X[t] @ W13_e^T      (W13_e rows [0, I) gate, [I, 2I) up)
+ *     h      = bf16( silu(g) * u )
+ *     out[t] += topk_w[t][j] * (h @ W2_e^T)
+ *   out = bf16(sum over j, fp32, in slot order).
+ *   X        device bf16 [T][H];  topk_ids int32 [T][topk] (each in [0, E));
+ *   topk_w   fp32 [T][topk];
+ *   W13      NVFP4, batch E, rows 2I, K H, ROWMAJOR;
+ *   W2       NVFP4, batch E, rows H,  K I, ROWMAJOR;
+ *   out      device bf16 [T][H];
+ *   workspace >= nvfp4_workspace_size(NVFP4_OP_GROUPED_GEMM, T, H, I, E, topk).
+ * H and I must be multiples of 128. */
+int nvfp4_grouped_gemm(const void* X, int64_t T, int topk, const int32_t* topk_ids,
+                       const float* topk_w, nvfp4_tensor_t W13, nvfp4_tensor_t W2,
+                       void* out, void* workspace, size_t workspace_bytes,
+                       nvfp4_stream_t stream);
+
+/* Masked draft LM head: gathered-row GEMV with a fused argmax. The draft
+ * proposes only ids from a fixed subset of the vocabulary, so the head reads
+ * only those rows ("The masked head trick", Serving Qwen3.8-27B...):
+ *   logit[m][j] = sum_k H[m][k] * W_hat[idx[j]][k]   (fp32 accumulation)
+ *   out_ids[m]  = idx[argmax_j logit[m][j]], ties to the lowest vocabulary id
+ *   out_logit[m] = that maximum logit (fp32), if out_logit != NULL.
+ *   H      device bf16 [M][K];  W  NVFP4 [V][K], batch 1, ROWMAJOR;
+ *   idx    device int32 [n_idx], each in [0, V); NULL = every row (n_idx = V)
+ *   workspace >= nvfp4_workspace_size(NVFP4_OP_GATHER_ARGMAX, M, n_idx, K, 0, 0).
+ * K must be a multiple of 128; 1 <= M <= 32; n_idx >= 1. */
+int nvfp4_gather_gemv_argmax(const void* H, int64_t M, nvfp4_tensor_t W,
+                             const int32_t* idx, int64_t n_idx, int32_t* out_ids,
+                             float* out_logit, void* workspace, size_t workspace_bytes,
+                             nvfp4_stream_t stream);
+
+/* ---- helpers --------------------------------------------------------------- */
+
+/* Bytes of one matrix's block scales in the given layout. */
+size_t nvfp4_scales_bytes(int64_t rows, int64_t K, int scale_layout);
+
+/* Workspace bytes an operation needs (0 if none). Arguments by op:
+ *   QUANTIZE:      (rows, -, K, -, -)
+ *   GEMM_W4A16:    (M, N, K, -, -)
+ *   GEMM_W4A4:     (M, N, K, -, -)   (worst case: both operands ROWMAJOR)
+ *   GROUPED_GEMM:  (T, H, I, E, topk)
+ *   GATHER_ARGMAX: (M, n_idx, K, -, -) */
+size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t c, int64_t e, int64_t topk);
+
+/* Human-readable name of a status code (static storage). */
+const char* nvfp4_status_string(int status);
+
+/* Reads and clears the device status word that bounded on-device waits set
+ * when they give up (synchronises `stream`). *out = NVFP4_OK or
+ * NVFP4_ERR_TIMEOUT. */
+int nvfp4_read_device_status(int* out, nvfp4_stream_t stream);
+
+/* Self-test of the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier nothing will ever arrive on, giving up after `limit_ns`
+ * nanoseconds, and records the outcome in the device status word. Used by the
+ * tests to show that a wait that runs out returns an error instead of hanging. */
+int nvfp4_selftest_bounded_wait(int64_t limit_ns, nvfp4_stream_t stream);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int nvfp4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_H_ */

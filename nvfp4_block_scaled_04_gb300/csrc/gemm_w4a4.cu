@@ -1,0 +1,439 @@
+// W4A4 NVFP4 GEMM on the 5th-generation tensor cores (sm_103a):
+//   Y[m][n] = bf16( s_tA * s_tW * sum_k a[m][k] * w[n][k] )
+// with a, w the e2m1 * e4m3 block-scaled values - "Blackwell-native NVFP4 W4A4
+// execution" (52.6% More Tokens, 1.53x Less GPU Time: Production Inference
+// with Minima and Rafay). The block-scaled MMA multiplies the e2m1 codes and
+// the per-16 E4M3 scales and accumulates in fp32 in tensor memory; the
+// epilogue applies the two fp32 tensor scales and rounds to bf16.
+//
+// One CTA computes a 128 x 128 output tile:
+//   warp 0       TMA producer: A and W code tiles (128 rows x 128 bytes, 128B
+//                swizzle) and their block scales (already in the MMA scale
+//                layout: one 512-byte atom per 128 rows x 64 K) into a
+//                3-stage shared-memory ring
+//   warp 1       allocates tensor memory; one lane copies the stage's scale
+//                atoms into tensor memory (tcgen05.cp) and issues
+//                tcgen05.mma.kind::mxf4nvf4 (M=128, N=128, K=64 each)
+//   warps 2..5   epilogue: tcgen05.ld of the fp32 accumulator, scale, bf16
+// Every mbarrier wait is bounded; a wait that gives up records
+// NVFP4_ERR_TIMEOUT in a device status word and the CTA unwinds, frees its
+// tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace nvfp4 {
+
+__device__ int g_device_status = 0;
+
+namespace {
+
+constexpr int BM = 128, BN = 128;
+constexpr int BK = 256;                // K elements per stage (128 bytes of codes)
+constexpr int STAGES = 3;
+constexpr int THREADS = 192;
+constexpr int TILE_BYTES = 128 * 128;  // one 128-row x 128-byte code tile
+constexpr int SF_BYTES = 4 * 512;      // four scale atoms per stage
+constexpr int STAGE_BYTES = 2 * TILE_BYTES + 2 * SF_BYTES;
+constexpr int TMEM_COLS = 256;         // 128 accumulator + 3 x 32 scale columns
+constexpr int SF_TMEM_BASE = 128;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int BAND = 32;               // m-tiles that share one sweep over the W tiles
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+
+// Instruction descriptor: kind::mxf4nvf4, A and B E2M1 (1), both K-major,
+// N>>3 at bit 17, UE4M3 scales (bit 23 = 0), M>>4 at bit 24.
+constexpr uint32_t IDESC = (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+NVFP4_DEV uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+NVFP4_DEV void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+NVFP4_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for `parity` on `bar`, giving up after limit_ns (or when another role
+// has already given up). Returns false on give-up.
+NVFP4_DEV bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                 unsigned long long limit_ns = WAIT_LIMIT_NS) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 0;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63) == 63) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        atomicExch(&g_device_status, NVFP4_ERR_TIMEOUT);
+        if (abort_flag) *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+NVFP4_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+NVFP4_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+NVFP4_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start >> 4 at bit 0, leading
+// byte offset >> 4 at bit 16, stride byte offset >> 4 at bit 32, version 1
+// at bit 46, layout (swizzle mode) at bit 61.
+NVFP4_DEV uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  return (uint64_t((addr & 0x3FFFFu) >> 4)) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (uint64_t(layout) << 61);
+}
+
+NVFP4_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+NVFP4_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+NVFP4_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+NVFP4_DEV void tc_mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                               uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+NVFP4_DEV void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+NVFP4_DEV void tc_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct W4A4Params {
+  const uint8_t* sfa;   // MMA-layout scales of A
+  const uint8_t* sfb;   // MMA-layout scales of W
+  const float* st_a;
+  const float* st_b;
+  uint16_t* Y;
+  int M, N, K;
+  int m_tiles, n_tiles;
+};
+
+__global__ void __launch_bounds__(THREADS, 2)
+    gemm_w4a4_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                     const W4A4Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128B-swizzled tiles
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bar_base = base + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES);
+  // bars[0..S) full, [S..2S) empty, [2S] accumulator ready
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 2);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  const uint32_t acc_bar = bar_base + 8u * (2 * STAGES);
+  auto stage_a = [&](int s) { return base + s * STAGE_BYTES; };
+  auto stage_b = [&](int s) { return base + s * STAGE_BYTES + TILE_BYTES; };
+  auto stage_sfa = [&](int s) { return base + s * STAGE_BYTES + 2 * TILE_BYTES; };
+  auto stage_sfb = [&](int s) { return base + s * STAGE_BYTES + 2 * TILE_BYTES + SF_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // tile of this CTA: bands of BAND m-tiles sweep all n-tiles, m fastest
+  const int b = blockIdx.x;
+  const int band = b / (BAND * p.n_tiles);
+  const int band_m0 = band * BAND;
+  const int band_h = min(BAND, p.m_tiles - band_m0);
+  const int within = b - band * BAND * p.n_tiles;
+  const int m_tile = band_m0 + within % band_h;
+  const int n_tile = within / band_h;
+  const int m0 = m_tile * BM, n0 = n_tile * BN;
+  const int n_k = (p.K + BK - 1) / BK;
+  const int k_atoms_total = p.K / 64;
+  const int64_t sf_row_stride = static_cast<int64_t>(k_atoms_total) * 512;   // bytes per 128-row scale strip
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(acc_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_a) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_b) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  int issued = 0;       // stages whose loads the producer issued
+  bool mma_started = false;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int ks = 0; ks < n_k; ++ks) {
+        const int s = ks % STAGES;
+        if (ks >= STAGES && !mbar_wait_bounded(empty_bar(s), ((ks / STAGES) - 1) & 1, abort_flag)) break;
+        const int atoms = min(4, k_atoms_total - 4 * ks);
+        const uint32_t sf_bytes = static_cast<uint32_t>(atoms) * 512u;
+        mbar_arrive_expect_tx(full_bar(s), 2u * TILE_BYTES + 2u * sf_bytes);
+        tma_load_2d(stage_a(s), &map_a, ks * 128, m0, full_bar(s));
+        tma_load_2d(stage_b(s), &map_b, ks * 128, n0, full_bar(s));
+        bulk_load(stage_sfa(s), p.sfa + m_tile * sf_row_stride + static_cast<int64_t>(ks) * SF_BYTES, sf_bytes,
+                  full_bar(s));
+        bulk_load(stage_sfb(s), p.sfb + n_tile * sf_row_stride + static_cast<int64_t>(ks) * SF_BYTES, sf_bytes,
+                  full_bar(s));
+        ++issued;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int ks = 0; ks < n_k; ++ks) {
+        const int s = ks % STAGES;
+        if (!mbar_wait_bounded(full_bar(s), (ks / STAGES) & 1, abort_flag)) break;
+        tc_fence_after();
+        const int atoms = min(4, k_atoms_total - 4 * ks);
+        const uint32_t sf_col = tmem + SF_TMEM_BASE + s * 32;
+        for (int k = 0; k < atoms; ++k) {
+          tc_cp_sf(sf_col + 4 * k, smem_desc(stage_sfa(s) + 512 * k, 128, 128, 0));
+          tc_cp_sf(sf_col + 16 + 4 * k, smem_desc(stage_sfb(s) + 512 * k, 128, 128, 0));
+        }
+        for (int k = 0; k < atoms; ++k) {
+          const uint64_t adesc = smem_desc(stage_a(s) + 32 * k, 16, 1024, 2);
+          const uint64_t bdesc = smem_desc(stage_b(s) + 32 * k, 16, 1024, 2);
+          tc_mma_mxf4nvf4(tmem, adesc, bdesc, IDESC, sf_col + 4 * k, sf_col + 16 + 4 * k,
+                          (ks > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_started = true;
+        tc_commit(empty_bar(s));
+      }
+      tc_commit(acc_bar);
+    }
+  } else {
+    // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, one output row per thread
+    const int quarter = warp & 3;
+    const int row = m0 + quarter * 32 + lane;
+    if (mbar_wait_bounded(acc_bar, 0, abort_flag)) {
+      tc_fence_after();
+      const float scale = p.st_a[0] * p.st_b[0];
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tc_ld_32cols(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 32u * c, r);
+        const int col0 = n0 + 32 * c;
+        if (row < p.M && col0 < p.N) {
+          uint16_t* dst = p.Y + static_cast<int64_t>(row) * p.N + col0;
+          if (col0 + 32 <= p.N) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 v;
+              v.x = f32x2_to_bf16x2(__uint_as_float(r[8 * q + 0]) * scale, __uint_as_float(r[8 * q + 1]) * scale);
+              v.y = f32x2_to_bf16x2(__uint_as_float(r[8 * q + 2]) * scale, __uint_as_float(r[8 * q + 3]) * scale);
+              v.z = f32x2_to_bf16x2(__uint_as_float(r[8 * q + 4]) * scale, __uint_as_float(r[8 * q + 5]) * scale);
+              v.w = f32x2_to_bf16x2(__uint_as_float(r[8 * q + 6]) * scale, __uint_as_float(r[8 * q + 7]) * scale);
+              reinterpret_cast<uint4*>(dst)[q] = v;
+            }
+          } else {
+            for (int j = 0; j < p.N - col0; ++j)
+              dst[j] = static_cast<uint16_t>(f32_to_bf16_bits(__uint_as_float(r[j]) * scale));
+          }
+        }
+      }
+    }
+  }
+
+  // Unwind. If a wait gave up, let the copies and MMAs already issued finish
+  // (bounded) before the shared and tensor memory they target go away.
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    for (int ks = 0; ks < issued; ++ks)
+      mbar_wait_bounded(full_bar(ks % STAGES), (ks / STAGES) & 1, nullptr, 100000000ull);
+  }
+  if (warp == 1 && lane == 0 && *abort_flag && mma_started) {
+    mbar_wait_bounded(acc_bar, 0, nullptr, 100000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// One CTA waits on an mbarrier that nothing arrives on: the bounded wait must
+// give up, record NVFP4_ERR_TIMEOUT and free the tensor memory it took.
+__global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t slot;
+  __shared__ int abort_flag;
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&slot)), "r"(32)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) mbar_wait_bounded(b, 0, &abort_flag, limit_ns);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(slot), "r"(32) : "memory");
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D map over packed codes [rows][K/2] bytes, 128 x 128-byte boxes, 128B swizzle.
+int make_code_map(CUtensorMap* map, const uint8_t* codes, int64_t rows, int64_t K) {
+  auto encode = get_encode();
+  if (!encode) return NVFP4_ERR_CUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+}  // namespace
+
+size_t w4a4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  return align_up(static_cast<size_t>(mma_scale_rows(M) * mma_scale_cols(K))) +
+         align_up(static_cast<size_t>(mma_scale_rows(N) * mma_scale_cols(K)));
+}
+
+int launch_gemm_w4a4(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t* Y, void* ws,
+                     cudaStream_t stream) {
+  const int64_t M = A.rows, N = W.rows, K = A.K;
+  if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  const uint8_t* sfa = A.scales;
+  const uint8_t* sfb = W.scales;
+  char* w = static_cast<char*>(ws);
+  if (A.scale_layout == NVFP4_SCALES_ROWMAJOR) {
+    uint8_t* dst = reinterpret_cast<uint8_t*>(w);
+    int rc = launch_prepack_scales(A.scales, 1, M, K, dst, stream);
+    if (rc != NVFP4_OK) return rc;
+    sfa = dst;
+  }
+  if (W.scale_layout == NVFP4_SCALES_ROWMAJOR) {
+    uint8_t* dst =
+        reinterpret_cast<uint8_t*>(w + align_up(static_cast<size_t>(mma_scale_rows(M) * mma_scale_cols(K))));
+    int rc = launch_prepack_scales(W.scales, 1, N, K, dst, stream);
+    if (rc != NVFP4_OK) return rc;
+    sfb = dst;
+  }
+  CUtensorMap map_a, map_b;
+  int rc = make_code_map(&map_a, A.codes, M, K);
+  if (rc != NVFP4_OK) return rc;
+  rc = make_code_map(&map_b, W.codes, N, K);
+  if (rc != NVFP4_OK) return rc;
+
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(gemm_w4a4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+        cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    attr_set = true;
+  }
+  W4A4Params p{};
+  p.sfa = sfa;
+  p.sfb = sfb;
+  p.st_a = A.s_t;
+  p.st_b = W.s_t;
+  p.Y = Y;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.m_tiles = static_cast<int>(ceil_div(M, BM));
+  p.n_tiles = static_cast<int>(ceil_div(N, BN));
+  const unsigned grid = static_cast<unsigned>(p.m_tiles) * static_cast<unsigned>(p.n_tiles);
+  gemm_w4a4_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(map_a, map_b, p);
+  return from_cuda(cudaGetLastError());
+}
+
+int read_device_status(int* out, cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  *out = v;
+  return NVFP4_OK;
+}
+
+int selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(limit_ns));
+  return from_cuda(cudaGetLastError());
+}
+
+}  // namespace nvfp4

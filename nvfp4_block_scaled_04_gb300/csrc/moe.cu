@@ -1,0 +1,261 @@
+// Routed-expert MoE layer, W4A16 (What 350+ Experiments Taught Us About
+// Serving Qwen 3.6 35B-A3B, sections 1 and 7: the routed-expert layout and an
+// NVFP4 mixture-of-experts kernel):
+//   route:    top-k of softmax(router logits), ties to the lower expert id
+//   plan:     group the T*k routed rows by expert, each expert padded to a
+//             multiple of 32 rows (one token chunk of the skinny kernel)
+//   gate/up:  [g; u] = x @ W13_e^T, h = bf16(silu(g) * u)      (skinny kernel)
+//   down:     y = h @ W2_e^T, fp32                              (skinny kernel)
+//   combine:  out[t] = bf16(sum_j w[t][j] * y[pos(t, j)]), slots in order
+// The order in which routed rows land inside an expert's group comes from
+// atomics, but every row's arithmetic is independent of its position, so the
+// output is deterministic.
+#include "gemv_core.cuh"
+#include "launch.h"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// One warp per token: fp32 softmax over E experts, then k rounds of "largest
+// (p, -id) below the previous winner".
+__global__ void route_kernel(const float* logits, int64_t T, int E, int topk, int32_t* ids, float* weights) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* l = logits + t * E;
+  float mx = -INFINITY;
+  for (int e = lane; e < E; e += 32) mx = fmaxf(mx, l[e]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum = 0.f;
+  for (int e = lane; e < E; e += 32) sum += expf(l[e] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  unsigned long long prev = ~0ull;
+  for (int j = 0; j < topk; ++j) {
+    unsigned long long best = 0ull;
+    for (int e = lane; e < E; e += 32) {
+      const float p = expf(l[e] - mx) / sum;
+      const unsigned long long key =
+          (static_cast<unsigned long long>(float_order_key(p)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e));
+      if (key < prev && key > best) best = key;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
+    }
+    prev = best;
+    if (lane == 0) {
+      ids[t * topk + j] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(best));
+      weights[t * topk + j] = float_from_order_key(static_cast<uint32_t>(best >> 32));
+    }
+  }
+}
+
+struct MoeWs {
+  int* counts;        // [E]
+  int* cursor;        // [E]
+  int* chunk_count;   // [1]
+  int* poff;          // [E]
+  int* chunk_expert;  // [max_chunks]
+  int* chunk_rows;    // [max_chunks]
+  int* row_of;        // [padded rows] token id or -1
+  int* pos_of;        // [T*k]
+  int* pexp1;         // [padded rows]
+  int* pexp2;         // [padded rows]
+  uint4* xfrag1;      // tokens, K = H
+  uint16_t* hbuf;     // [padded rows][I] bf16
+  uint4* xfrag2;      // h, K = I
+  float* ybuf;        // [padded rows][H] fp32
+  size_t zero_bytes;  // counts + cursor
+  size_t bytes;
+  int64_t max_chunks;
+};
+
+MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
+  MoeWs w{};
+  const int64_t R = T * topk;
+  w.max_chunks = ceil_div(R, GV_MCHUNK) + E;
+  const int64_t rows = w.max_chunks * GV_MCHUNK;
+  char* b = static_cast<char*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* p = b + off;
+    off += align_up(bytes);
+    return p;
+  };
+  w.counts = reinterpret_cast<int*>(take(E * sizeof(int)));
+  w.cursor = reinterpret_cast<int*>(take(E * sizeof(int)));
+  w.zero_bytes = off;
+  w.chunk_count = reinterpret_cast<int*>(take(sizeof(int)));
+  w.poff = reinterpret_cast<int*>(take(E * sizeof(int)));
+  w.chunk_expert = reinterpret_cast<int*>(take(w.max_chunks * sizeof(int)));
+  w.chunk_rows = reinterpret_cast<int*>(take(w.max_chunks * sizeof(int)));
+  w.row_of = reinterpret_cast<int*>(take(rows * sizeof(int)));
+  w.pos_of = reinterpret_cast<int*>(take(R * sizeof(int)));
+  w.pexp1 = reinterpret_cast<int*>(take(rows * sizeof(int)));
+  w.pexp2 = reinterpret_cast<int*>(take(rows * sizeof(int)));
+  w.xfrag1 = reinterpret_cast<uint4*>(take(xfrag_bytes(w.max_chunks, H)));
+  w.hbuf = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(rows) * I * sizeof(uint16_t)));
+  w.xfrag2 = reinterpret_cast<uint4*>(take(xfrag_bytes(w.max_chunks, I)));
+  w.ybuf = reinterpret_cast<float*>(take(static_cast<size_t>(rows) * H * sizeof(float)));
+  w.bytes = off;
+  return w;
+}
+
+__global__ void count_kernel(const int32_t* ids, int64_t R, int E, int* counts) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < R) {
+    const int e = ids[i];
+    if (e >= 0 && e < E) atomicAdd(&counts[e], 1);
+  }
+}
+
+// Single CTA: padded offsets, the chunk table, and row_of = -1 everywhere.
+__global__ void plan_kernel(const int* counts, int E, int* poff, int* chunk_count, int* chunk_expert,
+                            int* chunk_rows, int* row_of) {
+  __shared__ int s_total;
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      poff[e] = acc;
+      acc += (counts[e] + GV_MCHUNK - 1) / GV_MCHUNK * GV_MCHUNK;
+    }
+    s_total = acc;
+    *chunk_count = acc / GV_MCHUNK;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int n = counts[e];
+    const int c0 = poff[e] / GV_MCHUNK;
+    for (int c = 0; c * GV_MCHUNK < n; ++c) {
+      chunk_expert[c0 + c] = e;
+      chunk_rows[c0 + c] = min(GV_MCHUNK, n - c * GV_MCHUNK);
+    }
+  }
+  for (int r = threadIdx.x; r < s_total; r += blockDim.x) row_of[r] = -1;
+}
+
+__global__ void scatter_kernel(const int32_t* ids, int64_t R, int topk, int E, const int* poff, int* cursor,
+                               int* row_of, int* pos_of) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= R) return;
+  const int e = ids[i];
+  if (e < 0 || e >= E) {
+    pos_of[i] = -1;
+    return;
+  }
+  const int pos = poff[e] + atomicAdd(&cursor[e], 1);
+  row_of[pos] = static_cast<int>(i / topk);
+  pos_of[i] = pos;
+}
+
+// One CTA per padded row: gather (tokens) or pass through (h), to fragments.
+__global__ void __launch_bounds__(GV_THREADS) xprep_moe_kernel(const uint16_t* src, int64_t K, bool gather,
+                                                                const int* row_of, const int* chunk_count,
+                                                                uint4* xfrag, int* pexp) {
+  const int64_t r = blockIdx.x;
+  if (r >= static_cast<int64_t>(*chunk_count) * GV_MCHUNK) return;
+  const int tok = row_of[r];
+  const uint16_t* s = nullptr;
+  if (tok >= 0) s = gather ? src + static_cast<int64_t>(tok) * K : src + r * K;
+  xprep_row(s, K, r, xfrag, pexp);
+}
+
+__global__ void combine_kernel(const float* ybuf, const int* pos_of, const float* w, int64_t T, int topk,
+                               int64_t H, uint16_t* out) {
+  const int64_t t = blockIdx.x;
+  for (int64_t c = threadIdx.x; c < H; c += blockDim.x) {
+    float acc = 0.f;
+    for (int j = 0; j < topk; ++j) {
+      const int pos = pos_of[t * topk + j];
+      if (pos >= 0) acc = fmaf(w[t * topk + j], ybuf[static_cast<int64_t>(pos) * H + c], acc);
+    }
+    out[t * H + c] = static_cast<uint16_t>(f32_to_bf16_bits(acc));
+  }
+}
+
+}  // namespace
+
+int launch_moe_route(const float* logits, int64_t T, int E, int topk, int32_t* ids, float* weights,
+                     cudaStream_t stream) {
+  if (T == 0) return NVFP4_OK;
+  const int warps = 8;
+  route_kernel<<<static_cast<unsigned>(ceil_div(T, warps)), warps * 32, 0, stream>>>(logits, T, E, topk, ids,
+                                                                                   weights);
+  return from_cuda(cudaGetLastError());
+}
+
+size_t grouped_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
+  return carve_moe(nullptr, T, H, I, E, topk).bytes;
+}
+
+int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* ids, const float* w,
+                        const nvfp4_tensor_t& W13, const nvfp4_tensor_t& W2, uint16_t* out, void* ws,
+                        cudaStream_t stream) {
+  if (T == 0) return NVFP4_OK;
+  const int64_t E = W13.batch, I = W13.rows / 2, H = W13.K;
+  const int64_t R = T * topk;
+  const MoeWs m = carve_moe(ws, T, H, I, E, topk);
+  if (cudaMemsetAsync(m.counts, 0, m.zero_bytes, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+  const unsigned gr = static_cast<unsigned>(ceil_div(R, 256));
+  count_kernel<<<gr, 256, 0, stream>>>(ids, R, static_cast<int>(E), m.counts);
+  plan_kernel<<<1, 1024, 0, stream>>>(m.counts, static_cast<int>(E), m.poff, m.chunk_count, m.chunk_expert,
+                                      m.chunk_rows, m.row_of);
+  scatter_kernel<<<gr, 256, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.cursor, m.row_of,
+                                         m.pos_of);
+  const unsigned prow = static_cast<unsigned>(m.max_chunks * GV_MCHUNK);
+  xprep_moe_kernel<<<prow, GV_THREADS, 0, stream>>>(X, H, true, m.row_of, m.chunk_count, m.xfrag1, m.pexp1);
+  int rc = from_cuda(cudaGetLastError());
+  if (rc != NVFP4_OK) return rc;
+
+  SkinnyParams p{};
+  p.codes = W13.codes;
+  p.scales = W13.scales;
+  p.s_t = W13.s_t;
+  p.K = H;
+  p.xfrag = m.xfrag1;
+  p.pexp = m.pexp1;
+  p.split = 1;
+  p.chunk_count = m.chunk_count;
+  p.chunk_expert = m.chunk_expert;
+  p.chunk_rows = m.chunk_rows;
+  p.inter = I;
+  p.hidden = H;
+  p.rows_per_expert = 2 * I;
+  p.h_out = m.hbuf;
+  rc = launch_cluster(skinny_kernel<4, SK_MOE_GATEUP>,
+                      dim3(static_cast<unsigned>(m.max_chunks), static_cast<unsigned>(I / 64)), dim3(GV_THREADS),
+                      0, 1, stream, p);
+  if (rc != NVFP4_OK) return rc;
+
+  xprep_moe_kernel<<<prow, GV_THREADS, 0, stream>>>(m.hbuf, I, false, m.row_of, m.chunk_count, m.xfrag2,
+                                                    m.pexp2);
+  rc = from_cuda(cudaGetLastError());
+  if (rc != NVFP4_OK) return rc;
+
+  SkinnyParams q = p;
+  q.codes = W2.codes;
+  q.scales = W2.scales;
+  q.s_t = W2.s_t;
+  q.K = I;
+  q.xfrag = m.xfrag2;
+  q.pexp = m.pexp2;
+  q.rows_per_expert = H;
+  q.h_out = nullptr;
+  q.y_out = m.ybuf;
+  rc = launch_cluster(skinny_kernel<4, SK_MOE_DOWN>,
+                      dim3(static_cast<unsigned>(m.max_chunks), static_cast<unsigned>(ceil_div(H, GV_ROWS))),
+                      dim3(GV_THREADS), 0, 1, stream, q);
+  if (rc != NVFP4_OK) return rc;
+
+  combine_kernel<<<static_cast<unsigned>(T), 256, 0, stream>>>(m.ybuf, m.pos_of, w, T, topk, H, out);
+  return from_cuda(cudaGetLastError());
+}
+
+}  // namespace nvfp4

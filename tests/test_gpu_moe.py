@@ -1,0 +1,93 @@
+"""Routed-expert MoE layer: routing kernel and grouped expert GEMMs against
+the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from tests.gpu_common import DEV, np_f64, nv
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+def test_route_matches_oracle():
+    m = nv()
+    logits = synth.normal_f32((512, 128), 1.0, seed=8)
+    ids, w = m.moe_route(logits.to(DEV), 8)
+    oids, ow = O.moe_route(logits.numpy(), 8)
+    ids, w = ids.cpu().numpy(), w.cpu().numpy()
+    p = torch.softmax(logits.double(), 1).numpy()
+    for t in range(512):
+        ps = np.sort(p[t])[::-1]
+        gaps = np.abs(np.diff(ps[:9]))
+        if gaps.min() > 1e-6:            # no near-tie among the top 9
+            assert list(ids[t]) == list(oids[t])
+        np.testing.assert_allclose(w[t], p[t, ids[t]], rtol=1e-5)
+
+
+def moe_case(T, E, H, I, k, seed):
+    g = torch.Generator().manual_seed(seed)
+    logits = torch.randn(T, E, generator=g)
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    w13 = [torch.randn(2 * I, H, generator=g) * 0.02 for _ in range(E)]
+    w2 = [torch.randn(H, I, generator=g) * 0.02 for _ in range(E)]
+    return logits, x, w13, w2
+
+
+def run_gpu(logits, x, w13, w2, k, ids=None, wts=None):
+    m = nv()
+    if ids is None:
+        ids, wts = m.moe_route(logits.to(DEV), k)
+    q13 = m.quantize_stack([t.to(DEV) for t in w13])
+    q2 = m.quantize_stack([t.to(DEV) for t in w2])
+    return np_f64(m.grouped_gemm(x.to(DEV), ids, wts, q13, q2)), ids, wts
+
+
+@pytest.mark.parametrize("T,E,H,I,k", [(16, 4, 128, 128, 2), (100, 8, 256, 128, 3), (37, 16, 128, 256, 8)])
+def test_small_layers(T, E, H, I, k):
+    logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=T)
+    out, ids, wts = run_gpu(logits, x, w13, w2, k)
+    ref = O.moe_forward(x.float().numpy(), ids.cpu().numpy(), wts.cpu().numpy().astype(np.float64),
+                        [O.quantize(t.numpy()) for t in w13], [O.quantize(t.numpy()) for t in w2])
+    assert O.rel_fro(out, ref) <= TOL
+
+
+def test_skewed_routing_all_tokens_to_one_expert():
+    T, E, H, I = 70, 4, 128, 128
+    logits, x, w13, w2 = moe_case(T, E, H, I, 1, seed=3)
+    ids = torch.full((T, 1), 2, dtype=torch.int32, device=DEV)
+    wts = torch.ones(T, 1, device=DEV)
+    out, _, _ = run_gpu(logits, x, w13, w2, 1, ids, wts)
+    ref = O.moe_forward(x.float().numpy(), np.full((T, 1), 2), np.ones((T, 1)),
+                        [O.quantize(t.numpy()) for t in w13], [O.quantize(t.numpy()) for t in w2])
+    assert O.rel_fro(out, ref) <= TOL
+
+
+def test_deterministic_across_calls():
+    logits, x, w13, w2 = moe_case(64, 8, 128, 128, 4, seed=5)
+    a, ids, wts = run_gpu(logits, x, w13, w2, 4)
+    b, _, _ = run_gpu(logits, x, w13, w2, 4, ids, wts)
+    assert np.array_equal(a, b)
+
+
+def test_moe_config_t256_sampled_tokens():
+    """The 35B-A3B-shaped layer (128 experts, top-8, H=2048, I=768) at T=256:
+    64 sampled tokens recomputed by the oracle from its own routing."""
+    m = nv()
+    T = 256
+    logits, x, w13, w2 = synth.moe_inputs(T)
+    ids, wts = m.moe_route(logits.to(DEV), 8)
+    q13 = m.quantize_stack([w13[e].to(DEV) for e in range(128)])
+    q2 = m.quantize_stack([w2[e].to(DEV) for e in range(128)])
+    out = np_f64(m.grouped_gemm(x.to(DEV), ids, wts, q13, q2))
+    oids, ow = O.moe_route(logits.numpy(), 8)
+    toks = np.sort(np.random.default_rng(1).choice(T, 64, replace=False))
+    used = sorted(set(oids[toks].ravel().tolist()))
+    r13 = {e: O.quantize(w13[e].numpy()) for e in used}
+    r2 = {e: O.quantize(w2[e].numpy()) for e in used}
+    ref = O.moe_forward(x.float().numpy()[toks], oids[toks], ow[toks],
+                        [r13.get(e, r13[used[0]]) for e in range(128)],
+                        [r2.get(e, r2[used[0]]) for e in range(128)])
+    assert O.rel_fro(out[toks], ref) <= TOL

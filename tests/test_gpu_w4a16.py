@@ -1,0 +1,78 @@
+"""W4A16 decode GEMV / skinny GEMM parity against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from tests.gpu_common import DEV, np_f64, nv
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+def run(w_f32, x_bf16):
+    m = nv()
+    qw = m.quantize(w_f32.to(DEV))
+    y = m.gemm_w4a16(x_bf16.to(DEV), qw)
+    return np_f64(y), O.gemm_w4a16(x_bf16.float().numpy(), O.quantize(w_f32.numpy()))
+
+
+def test_tiny_config():
+    w, x = synth.tiny_w4a16(seed=0)
+    y, ref = run(w, x)
+    assert O.rel_fro(y, ref) <= TOL
+    assert np.max(np.abs(y - ref)) / np.max(np.abs(ref)) <= TOL
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 9, 17, 32, 33, 70])
+@pytest.mark.parametrize("N,K", [(512, 256), (200, 384), (136, 1280)])
+def test_shapes(M, N, K):
+    w = synth.normal_f32((N, K), 0.02, seed=N + K)
+    x = synth.normal_bf16((M, K), seed=M)
+    y, ref = run(w, x)
+    assert O.rel_fro(y, ref) <= TOL, (M, N, K)
+
+
+def test_exact_special_case_is_bit_exact():
+    """Power-of-two scales, s_t = 1, activations in {-8..8}/8: every partial
+    sum is exact in fp32, so the bf16 output must equal the rounded fp64 sum."""
+    m = nv()
+    rng = np.random.default_rng(1)
+    N, K, M = 512, 256, 4
+    codes = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    exps = rng.integers(-3, 4, (N, K // 16))
+    scales = (((exps + 7) << 3)).astype(np.uint8)
+    qref = O.QTensor(O.pack_codes(codes), scales, 1.0)
+    x = torch.from_numpy(rng.integers(-8, 9, (M, K)).astype(np.float32) / 8).to(torch.bfloat16)
+    qw = m.QTensor(torch.from_numpy(qref.codes).to(DEV), torch.from_numpy(qref.scales).to(DEV),
+                   torch.ones(1, device=DEV), N, K)
+    y = m.gemm_w4a16(x.to(DEV), qw).float().cpu().numpy()
+    ref = O.bf16_round(O.gemm_w4a16(x.float().numpy(), qref))
+    assert np.array_equal(y, ref)
+
+
+def test_large_activation_range():
+    """Activations far outside f16 range (and tiny ones) still match."""
+    w = synth.normal_f32((256, 512), 0.02, seed=3)
+    x = (synth.normal_f32((4, 512), 1.0, seed=4) * torch.tensor([[1e6], [1e-6], [3e30], [1.0]])).to(torch.bfloat16)
+    y, ref = run(w, x)
+    for r in range(4):
+        assert O.rel_fro(y[r], ref[r]) <= TOL
+
+
+@pytest.mark.parametrize("which", ["gate_up", "down"])
+@pytest.mark.parametrize("M", [1, 4, 8, 32])
+def test_decode_config_sampled_rows(which, M):
+    """27B decode linears at full size, the bench's launch; output columns
+    sampled and recomputed by the oracle one by one."""
+    m = nv()
+    w = synth.decode_weight(which)
+    N, K = w.shape
+    x = synth.decode_activation(M, K)
+    qw = m.quantize(w.to(DEV))
+    y = np_f64(m.gemm_w4a16(x.to(DEV), qw))
+    cols = np.sort(np.random.default_rng(M).choice(N, 384, replace=False))
+    st = O.tensor_scale(w.numpy())
+    ref = O.gemm_w4a16(x.float().numpy(), O.quantize(w.numpy()[cols], s_t=st))
+    assert O.rel_fro(y[:, cols], ref) <= TOL

@@ -1,0 +1,78 @@
+"""W4A4 prefill GEMM on the block-scaled FP4 tensor cores, against the
+fp64 oracle on the oracle's own quantisation of the same inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from tests.gpu_common import DEV, np_f64, nv
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+def gpu_gemm(a_bf16, w_f32, a_layout=1, w_layout=1):
+    m = nv()
+    qa = m.quantize(a_bf16.to(DEV), scale_layout=a_layout)
+    qw = m.quantize(w_f32.to(DEV))
+    if w_layout == 1:
+        qw = m.prepack_scales(qw)
+    return np_f64(m.gemm_w4a4(qa, qw))
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 256, 512), (200, 136, 320), (1, 8, 64),
+                                   (384, 512, 1024), (130, 264, 576)])
+@pytest.mark.parametrize("layouts", [(1, 1), (0, 0)])
+def test_shapes(M, N, K, layouts):
+    a = synth.student_t_bf16((M, K), 4, seed=M)
+    w = synth.normal_f32((N, K), 0.02, seed=N)
+    y = gpu_gemm(a, w, *layouts)
+    ref = O.gemm_w4a4(O.quantize(a.float().numpy()), O.quantize(w.numpy()))
+    assert O.rel_fro(y, ref) <= TOL, (M, N, K, O.rel_fro(y, ref))
+
+
+def test_exact_special_case_is_bit_exact():
+    """Unit scales and s_t = 1 on both sides: products of e2m1 codes are exact
+    and every partial sum is a small multiple of 1/4, so the output is exact."""
+    m = nv()
+    rng = np.random.default_rng(2)
+    M, N, K = 128, 128, 256
+    ca = rng.integers(0, 16, (M, K)).astype(np.uint8)
+    cw = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    one = np.full((M, K // 16), 0x38, np.uint8)
+    qa_ref = O.QTensor(O.pack_codes(ca), one, 1.0)
+    qw_ref = O.QTensor(O.pack_codes(cw), np.full((N, K // 16), 0x38, np.uint8), 1.0)
+    dev = lambda a: torch.from_numpy(a).to(DEV)
+    qa = m.QTensor(dev(qa_ref.codes), dev(qa_ref.scales), torch.ones(1, device=DEV), M, K)
+    qw = m.QTensor(dev(qw_ref.codes), dev(qw_ref.scales), torch.ones(1, device=DEV), N, K)
+    y = np_f64(m.gemm_w4a4(qa, qw))
+    assert np.array_equal(y, O.bf16_round(O.gemm_w4a4(qa_ref, qw_ref)))
+
+
+def test_reduces_to_w4a16_on_decoded_activations():
+    m = nv()
+    a = synth.student_t_bf16((64, 512), 4, seed=5)
+    w = synth.normal_f32((256, 512), 0.02, seed=6)
+    y4 = gpu_gemm(a, w)
+    aq = O.quantize(a.float().numpy())
+    ref = O.gemm_w4a16(O.decode(aq), O.quantize(w.numpy()))
+    assert O.rel_fro(y4, ref) <= TOL
+
+
+def test_prefill_config_sampled():
+    """M=8192, K=5120, N=34816 at full size; 128 rows x 1024 columns of the
+    output recomputed by the oracle."""
+    m = nv()
+    a, w = synth.prefill_inputs()
+    qa = m.quantize(a.to(DEV), scale_layout=m.SCALES_MMA)
+    qw = m.prepack_scales(m.quantize(w.to(DEV)))
+    y = m.gemm_w4a4(qa, qw)
+    rng = np.random.default_rng(7)
+    rows = np.sort(rng.choice(a.shape[0], 128, replace=False))
+    cols = np.sort(rng.choice(w.shape[0], 1024, replace=False))
+    ys = np_f64(y[torch.from_numpy(rows).to(DEV)][:, torch.from_numpy(cols).to(DEV)])
+    a_np, w_np = a.float().numpy(), w.numpy()
+    ra = O.quantize(a_np[rows], s_t=O.tensor_scale(a_np))
+    rw = O.quantize(w_np[cols], s_t=O.tensor_scale(w_np))
+    assert O.rel_fro(ys, O.gemm_w4a4(ra, rw)) <= TOL
