@@ -1,4 +1,6 @@
 """Masked draft head (gathered-row GEMV + argmax) against the oracle."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -62,18 +64,23 @@ def test_planted_winner():
     assert int(ids[0]) == target
 
 
+@functools.lru_cache(maxsize=1)
+def _head():
+    """(fp32 head, mask, GPU quantisation, oracle tensor scale, oracle masked rows)."""
+    w = synth.draft_head_weight()
+    idx = synth.draft_mask()
+    st = O.tensor_scale(w.numpy())
+    return w, idx, nv().quantize(w.to(DEV)), st, O.quantize(w.numpy()[idx.numpy()], s_t=st)
+
+
 @pytest.mark.parametrize("M", [1, 4, 8])
 def test_draft_head_config(M):
     """248,320 x 5120 head, 32,768-id mask, 3 draft steps: the masked argmax
     is checked exactly against the oracle over all masked rows; the full-vocab
     argmax is checked by its value and by sampled rows."""
     m = nv()
-    w = synth.draft_head_weight()
-    idx = synth.draft_mask()
-    qw = m.quantize(w.to(DEV))
-    st = O.tensor_scale(w.numpy())
+    w, idx, qw, st, wq_masked = _head()
     idx_np = idx.numpy()
-    wq_masked = O.quantize(w.numpy()[idx_np], s_t=st)
     for step in range(3):
         h = synth.draft_hidden(M, step)
         ids, logit = m.gather_gemv_argmax(h.to(DEV), qw, idx.to(DEV))

@@ -1,4 +1,6 @@
 """W4A16 decode GEMV / skinny GEMM parity against the fp64 oracle."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -61,18 +63,23 @@ def test_large_activation_range():
         assert O.rel_fro(y[r], ref[r]) <= TOL
 
 
+@functools.lru_cache(maxsize=1)
+def _decode_weight(which):
+    """(fp32 weight, its GPU quantisation, the oracle's tensor scale)."""
+    w = synth.decode_weight(which)
+    return w, nv().quantize(w.to(DEV)), O.tensor_scale(w.numpy())
+
+
 @pytest.mark.parametrize("which", ["gate_up", "down"])
 @pytest.mark.parametrize("M", [1, 4, 8, 32])
 def test_decode_config_sampled_rows(which, M):
     """27B decode linears at full size, the bench's launch; output columns
     sampled and recomputed by the oracle one by one."""
     m = nv()
-    w = synth.decode_weight(which)
+    w, qw, st = _decode_weight(which)
     N, K = w.shape
     x = synth.decode_activation(M, K)
-    qw = m.quantize(w.to(DEV))
     y = np_f64(m.gemm_w4a16(x.to(DEV), qw))
     cols = np.sort(np.random.default_rng(M).choice(N, 384, replace=False))
-    st = O.tensor_scale(w.numpy())
     ref = O.gemm_w4a16(x.float().numpy(), O.quantize(w.numpy()[cols], s_t=st))
     assert O.rel_fro(y[:, cols], ref) <= TOL
