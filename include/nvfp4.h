@@ -48,6 +48,7 @@ typedef struct CUstream_st* nvfp4_stream_t;   /* == cudaStream_t */
 #define NVFP4_ERR_CUDA              -4   /* a CUDA runtime / driver call failed */
 #define NVFP4_ERR_WORKSPACE         -5   /* workspace missing or too small */
 #define NVFP4_ERR_TIMEOUT           -6   /* a bounded on-device wait gave up (device status word) */
+#define NVFP4_ERR_SCRATCH_LIMIT     -7   /* shape exceeds the fixed scratch of nvfp4_gemm_w4a16_noalloc */
 
 /* ---- enums --------------------------------------------------------------- */
 #define NVFP4_DTYPE_F32   0
@@ -128,6 +129,22 @@ int nvfp4_prepack_scales(const uint8_t* src, int64_t batch, int64_t rows, int64_
  * K must be a multiple of 128. Any M >= 1 (tuned for M <= 32). */
 int nvfp4_gemm_w4a16(const void* X, int64_t M, nvfp4_tensor_t W, void* Y,
                      void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* nvfp4_gemm_w4a16 without a workspace: the same computation and kernels, with
+ * the converted activations kept in a fixed 2 MiB + 4 KiB array of device
+ * memory inside the library instead of caller memory. The pages have no
+ * counterpart of this entry point; it serves callers that cannot allocate on
+ * their decode path - an engine that reserves nearly all device memory for its
+ * KV cache at start-up, or a host that must not call cudaMalloc / cudaFree
+ * there because those calls can synchronise the device.
+ *   X, M, W, Y as for nvfp4_gemm_w4a16; 1 <= M <= 32, K <= 32768, else
+ *   NVFP4_ERR_SCRATCH_LIMIT before anything is launched.
+ * The first call on each device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress; make it before any
+ * stream capture. All calls share the array: calls that overlap on the GPU
+ * race and must be serialised by the caller. Nothing in it needs zeroing. */
+int nvfp4_gemm_w4a16_noalloc(const void* X, int64_t M, nvfp4_tensor_t W, void* Y,
+                             nvfp4_stream_t stream);
 
 /* W4A4 linear (prefill): Y[m][n] = bf16( s_tA * s_tW * sum_k a[m][k] * w[n][k] )
  * where a, w are the e2m1*e4m3 products, multiplied and accumulated (fp32) by

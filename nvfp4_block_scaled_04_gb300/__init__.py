@@ -26,6 +26,7 @@ EXPORTS = [
     "nvfp4_moe_route", "nvfp4_grouped_gemm", "nvfp4_gather_gemv_argmax",
     "nvfp4_scales_bytes", "nvfp4_workspace_size", "nvfp4_status_string",
     "nvfp4_read_device_status", "nvfp4_selftest_bounded_wait", "nvfp4_version",
+    "nvfp4_gemm_w4a16_noalloc",
 ]
 _NON_INT = ("nvfp4_scales_bytes", "nvfp4_workspace_size", "nvfp4_status_string")
 
@@ -52,6 +53,7 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_prepack_scales.argtypes = [vp, i64, i64, i64, vp, vp]
         L.nvfp4_gemm_w4a16.argtypes = [vp, i64, CTensor, vp, vp, sz, vp]
         L.nvfp4_gemm_w4a4.argtypes = [CTensor, CTensor, vp, vp, sz, vp]
+        L.nvfp4_gemm_w4a16_noalloc.argtypes = [vp, i64, CTensor, vp, vp]
         L.nvfp4_moe_route.argtypes = [vp, i64, i32, i32, vp, vp, vp]
         L.nvfp4_grouped_gemm.argtypes = [vp, i64, i32, vp, vp, CTensor, CTensor, vp, vp, sz, vp]
         L.nvfp4_gather_gemv_argmax.argtypes = [vp, i64, CTensor, vp, i64, vp, vp, vp, sz, vp]

@@ -46,6 +46,7 @@ const char* nvfp4_status_string(int status) {
     case NVFP4_ERR_CUDA: return "CUDA error";
     case NVFP4_ERR_WORKSPACE: return "workspace missing or too small";
     case NVFP4_ERR_TIMEOUT: return "bounded on-device wait timed out";
+    case NVFP4_ERR_SCRATCH_LIMIT: return "shape exceeds the fixed scratch of the allocation-free entry point";
     default: return "unknown status";
   }
 }
