@@ -131,7 +131,7 @@ int nvfp4_gemm_w4a16(const void* X, int64_t M, nvfp4_tensor_t W, void* Y,
                      void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /* nvfp4_gemm_w4a16 without a workspace: the same computation and kernels, with
- * the converted activations kept in a fixed 2 MiB + 4 KiB array of device
+ * the converted activations and split-K partials kept in a fixed 8 MiB array of device
  * memory inside the library instead of caller memory. The pages have no
  * counterpart of this entry point; it serves callers that cannot allocate on
  * their decode path - an engine that reserves nearly all device memory for its

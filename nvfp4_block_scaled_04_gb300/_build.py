@@ -17,7 +17,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libnvfp4.so"
-SOURCES = ["api.cu", "quantize.cu", "gemv.cu", "moe.cu", "gemm_w4a4.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemv.cu", "moe.cu", "gemm_w4a4.cu", "noalloc.cu", "tma_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-Xptxas", "-warn-spills", f"-I{ROOT / 'include'}"]

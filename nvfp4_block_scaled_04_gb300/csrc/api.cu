@@ -3,6 +3,8 @@
 // computes on the CPU; an invalid call returns an error before any launch.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -19,6 +21,29 @@ int sm_count() {
     cached[dev] = n;
   }
   return cached[dev];
+}
+
+int ensure_smem_impl(const void* func, int bytes) {
+  static std::mutex mu;
+  static const void* funcs[256];
+  static unsigned long long devmask[256];
+  static int n = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+  const unsigned long long bit = 1ull << (dev & 63);
+  std::lock_guard<std::mutex> lock(mu);
+  int i = 0;
+  while (i < n && funcs[i] != func) ++i;
+  if (i < n && (devmask[i] & bit)) return NVFP4_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  if (i == n) {
+    if (n == 256) return NVFP4_OK;
+    funcs[n] = func;
+    devmask[n++] = 0;
+  }
+  devmask[i] |= bit;
+  return NVFP4_OK;
 }
 
 namespace {
@@ -61,7 +86,7 @@ size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t c, int64_t e, 
   if (a < 0 || b < 0 || c < 0 || e < 0 || topk < 0) return 0;
   switch (op) {
     case NVFP4_OP_QUANTIZE: return quantize_workspace_bytes();
-    case NVFP4_OP_GEMM_W4A16: return a > 0 && c > 0 ? w4a16_workspace_bytes(a, c) : 0;
+    case NVFP4_OP_GEMM_W4A16: return a > 0 && c > 0 ? w4a16_workspace_bytes(a, b, c) : 0;
     case NVFP4_OP_GEMM_W4A4: return w4a4_workspace_bytes(a, b, c);
     case NVFP4_OP_GROUPED_GEMM: return grouped_workspace_bytes(a, b, c, e, topk);
     case NVFP4_OP_GATHER_ARGMAX: return a > 0 && c > 0 ? argmax_workspace_bytes(a, c) : 0;
@@ -99,7 +124,7 @@ int nvfp4_gemm_w4a16(const void* X, int64_t M, nvfp4_tensor_t W, void* Y, void* 
   if (W.K % 128 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(X) || !aligned16(W.codes) || !aligned16(Y)) return NVFP4_ERR_MISALIGNED;
   if (M == 0 || W.rows == 0) return NVFP4_OK;
-  if (!workspace || workspace_bytes < w4a16_workspace_bytes(M, W.K)) return NVFP4_ERR_WORKSPACE;
+  if (!workspace || workspace_bytes < w4a16_workspace_bytes(M, W.rows, W.K)) return NVFP4_ERR_WORKSPACE;
   return launch_gemm_w4a16(static_cast<const uint16_t*>(X), M, W, static_cast<uint16_t*>(Y), workspace,
                            reinterpret_cast<cudaStream_t>(stream));
 }

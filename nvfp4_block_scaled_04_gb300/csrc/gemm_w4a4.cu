@@ -23,10 +23,23 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tc_util.cuh"
 
 namespace nvfp4 {
 
 __device__ int g_device_status = 0;
+
+int* device_status_ptr() {
+  static int* cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cached[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    cached[dev] = static_cast<int*>(p);
+  }
+  return cached[dev];
+}
 
 namespace {
 
@@ -41,78 +54,10 @@ constexpr int TMEM_COLS = 256;         // 128 accumulator + 3 x 32 scale columns
 constexpr int SF_TMEM_BASE = 128;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr int BAND = 32;               // m-tiles that share one sweep over the W tiles
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
 // Instruction descriptor: kind::mxf4nvf4, A and B E2M1 (1), both K-major,
 // N>>3 at bit 17, UE4M3 scales (bit 23 = 0), M>>4 at bit 24.
 constexpr uint32_t IDESC = (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
-
-NVFP4_DEV uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-NVFP4_DEV void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-NVFP4_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for `parity` on `bar`, giving up after limit_ns (or when another role
-// has already given up). Returns false on give-up.
-NVFP4_DEV bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                 unsigned long long limit_ns = WAIT_LIMIT_NS) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t n = 0;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 63) == 63) {
-      if (abort_flag && *abort_flag) return false;
-      if (globaltimer() - t0 > limit_ns) {
-        atomicExch(&g_device_status, NVFP4_ERR_TIMEOUT);
-        if (abort_flag) *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
-NVFP4_DEV void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-NVFP4_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-NVFP4_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
-// Shared-memory matrix descriptor (tcgen05): start >> 4 at bit 0, leading
-// byte offset >> 4 at bit 16, stride byte offset >> 4 at bit 32, version 1
-// at bit 46, layout (swizzle mode) at bit 61.
-NVFP4_DEV uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
-  return (uint64_t((addr & 0x3FFFFu) >> 4)) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
-         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (uint64_t(layout) << 61);
-}
 
 NVFP4_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 NVFP4_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -224,7 +169,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (lane == 0) {
       for (int ks = 0; ks < n_k; ++ks) {
         const int s = ks % STAGES;
-        if (ks >= STAGES && !mbar_wait_bounded(empty_bar(s), ((ks / STAGES) - 1) & 1, abort_flag)) break;
+        if (ks >= STAGES && !mbar_wait_bounded(empty_bar(s), ((ks / STAGES) - 1) & 1, abort_flag, &g_device_status)) break;
         const int atoms = min(4, k_atoms_total - 4 * ks);
         const uint32_t sf_bytes = static_cast<uint32_t>(atoms) * 512u;
         mbar_arrive_expect_tx(full_bar(s), 2u * TILE_BYTES + 2u * sf_bytes);
@@ -241,7 +186,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (lane == 0) {
       for (int ks = 0; ks < n_k; ++ks) {
         const int s = ks % STAGES;
-        if (!mbar_wait_bounded(full_bar(s), (ks / STAGES) & 1, abort_flag)) break;
+        if (!mbar_wait_bounded(full_bar(s), (ks / STAGES) & 1, abort_flag, &g_device_status)) break;
         tc_fence_after();
         const int atoms = min(4, k_atoms_total - 4 * ks);
         const uint32_t sf_col = tmem + SF_TMEM_BASE + s * 32;
@@ -264,7 +209,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, one output row per thread
     const int quarter = warp & 3;
     const int row = m0 + quarter * 32 + lane;
-    if (mbar_wait_bounded(acc_bar, 0, abort_flag)) {
+    if (mbar_wait_bounded(acc_bar, 0, abort_flag, &g_device_status)) {
       tc_fence_after();
       const float scale = p.st_a[0] * p.st_b[0];
 #pragma unroll 1
@@ -297,10 +242,10 @@ __global__ void __launch_bounds__(THREADS, 2)
   // (bounded) before the shared and tensor memory they target go away.
   if (warp == 0 && lane == 0 && *abort_flag) {
     for (int ks = 0; ks < issued; ++ks)
-      mbar_wait_bounded(full_bar(ks % STAGES), (ks / STAGES) & 1, nullptr, 100000000ull);
+      mbar_wait_bounded(full_bar(ks % STAGES), (ks / STAGES) & 1, nullptr, &g_device_status, 100000000ull);
   }
   if (warp == 1 && lane == 0 && *abort_flag && mma_started) {
-    mbar_wait_bounded(acc_bar, 0, nullptr, 100000000ull);
+    mbar_wait_bounded(acc_bar, 0, nullptr, &g_device_status, 100000000ull);
   }
   tc_fence_before();
   __syncthreads();
@@ -328,38 +273,16 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (threadIdx.x == 0) mbar_wait_bounded(b, 0, &abort_flag, limit_ns);
+  if (threadIdx.x == 0) mbar_wait_bounded(b, 0, &abort_flag, &g_device_status, limit_ns);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(slot), "r"(32) : "memory");
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 // 2-D map over packed codes [rows][K/2] bytes, 128 x 128-byte boxes, 128B swizzle.
 int make_code_map(CUtensorMap* map, const uint8_t* codes, int64_t rows, int64_t K) {
-  auto encode = get_encode();
-  if (!encode) return NVFP4_ERR_CUDA;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-  cuuint32_t box[2] = {128, 128};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+  return make_tmap_2d_u8(map, codes, K / 2, rows, K / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 constexpr size_t kAlign = 256;

@@ -2,6 +2,7 @@
 // GEMV with fused argmax. The mainloop lives in gemv_core.cuh; this file
 // sizes the launches and carves the workspace.
 #include "gemv_core.cuh"
+#include "gemv_tma.cuh"
 #include "launch.h"
 
 namespace nvfp4 {
@@ -10,10 +11,22 @@ namespace {
 
 // One CTA per output row of a dense activation matrix X[M][K] (rows beyond
 // M, up to the n-tile padding of the chunk, become zeros).
-__global__ void __launch_bounds__(GV_THREADS) xprep_dense_kernel(const uint16_t* X, int64_t M, int64_t K,
-                                                                  uint4* xfrag, int* pexp) {
+// CTA (0, 0) also zeroes the split-K arrival counters of the GEMV that follows.
+// 1024 threads per row: up to K = 32768 the row is read once, into registers.
+constexpr int XPREP_THREADS = 1024;
+__global__ void __launch_bounds__(XPREP_THREADS) xprep_dense_kernel(const uint16_t* X, int64_t M, int64_t K,
+                                                                     uint4* xfrag, int* pexp,
+                                                                     unsigned int* counters, int n_counters) {
+  pdl_launch_dependents();
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
   const int64_t out_row = static_cast<int64_t>(blockIdx.y) * GV_MCHUNK + blockIdx.x;
-  xprep_row(out_row < M ? X + out_row * K : nullptr, K, out_row, xfrag, pexp);
+  const uint16_t* src = out_row < M ? X + out_row * K : nullptr;
+  const int64_t n8 = K / 8;
+  if (n8 <= XPREP_THREADS) xprep_row_regs<1>(src, K, out_row, xfrag, pexp);
+  else if (n8 <= 2 * XPREP_THREADS) xprep_row_regs<2>(src, K, out_row, xfrag, pexp);
+  else if (n8 <= 4 * XPREP_THREADS) xprep_row_regs<4>(src, K, out_row, xfrag, pexp);
+  else xprep_row(src, K, out_row, xfrag, pexp);
 }
 
 constexpr size_t kAlign = 256;
@@ -41,15 +54,37 @@ int launch_skinny_nt(int nt, const SkinnyParams& p, dim3 grid, cudaStream_t stre
   }
 }
 
+// Two m-tiles per consumer warp once there are several n-tiles, so each
+// activation fragment read from shared memory feeds two MMAs.
+template <int NT>
+int launch_tma_plain_nt(const TmaSkinnyParams& p, const CUtensorMap& mc, const CUtensorMap& ms, dim3 grid,
+                        cudaStream_t stream) {
+  constexpr int MT = NT >= 2 ? 2 : 1;
+  constexpr int KW = NT >= 2 ? 2 : 1;   // measured: helps when the MMA work per stage is large
+  auto k = skinny_tma_kernel<NT, SK_PLAIN, MT, KW>;
+  int rc = ensure_smem(k, GtCfg<NT>::SMEM);
+  if (rc != NVFP4_OK) return rc;
+  return launch_ex(k, grid, dim3(GtWarps<MT, KW>::THREADS), GtCfg<NT>::SMEM, 1, true, stream, mc, ms, p);
+}
+
+// Split-K of the TMA-fed GEMV: as many K-slices per 128-row tile as still fit
+// in one wave of two CTAs per SM (at most 8, at least one stage each).
+int tma_split(int64_t tiles, int64_t n_stages) { return choose_split(tiles, n_stages); }
+
 struct DenseWs {
   int* pexp;
   uint4* xfrag;
   unsigned long long* keys;
   unsigned int* counter;
+  unsigned int* tile_counters;
+  int n_tile_counters;
+  float* partials;
   size_t bytes;
 };
 
-DenseWs carve_dense(void* base, int64_t M, int64_t K, bool argmax) {
+// Workspace: [argmax keys + counter] [per-token shifts] [split-K counters]
+// [split-K partials] [activation fragments].
+DenseWs carve_dense(void* base, int64_t M, int64_t N, int64_t K, bool argmax) {
   const int64_t chunks = ceil_div(M, GV_MCHUNK);
   DenseWs w{};
   size_t off = 0;
@@ -62,6 +97,18 @@ DenseWs carve_dense(void* base, int64_t M, int64_t K, bool argmax) {
   }
   w.pexp = reinterpret_cast<int*>(b + off);
   off += align_up(static_cast<size_t>(chunks) * GV_MCHUNK * sizeof(int));
+  if (!argmax && K % 256 == 0) {
+    // only a split tile needs counters and partials; then tiles * split <= 2 * SMs
+    const int64_t tiles = chunks * ceil_div(N, GV_ROWS);
+    const int S = tma_split(tiles, K / 256);
+    if (S > 1) {
+      w.n_tile_counters = static_cast<int>(tiles);
+      w.tile_counters = reinterpret_cast<unsigned int*>(b + off);
+      off += align_up(static_cast<size_t>(tiles) * sizeof(unsigned int));
+      w.partials = reinterpret_cast<float*>(b + off);
+      off += align_up(static_cast<size_t>(tiles) * S * GV_MCHUNK * GV_ROWS * sizeof(float));
+    }
+  }
   w.xfrag = reinterpret_cast<uint4*>(b + off);
   off += align_up(xfrag_bytes(chunks, K));
   w.bytes = off;
@@ -71,24 +118,52 @@ DenseWs carve_dense(void* base, int64_t M, int64_t K, bool argmax) {
 int prep_dense(const uint16_t* X, int64_t M, int64_t K, int nt, const DenseWs& w, cudaStream_t stream) {
   const int64_t chunks = ceil_div(M, GV_MCHUNK);
   dim3 grid(static_cast<unsigned>(8 * nt), static_cast<unsigned>(chunks));
-  xprep_dense_kernel<<<grid, GV_THREADS, 0, stream>>>(X, M, K, w.xfrag, w.pexp);
+  xprep_dense_kernel<<<grid, XPREP_THREADS, 0, stream>>>(X, M, K, w.xfrag, w.pexp, w.tile_counters,
+                                                         w.n_tile_counters);
   return from_cuda(cudaGetLastError());
 }
 
 }  // namespace
 
-size_t w4a16_workspace_bytes(int64_t M, int64_t K) { return carve_dense(nullptr, M, K, false).bytes; }
-size_t argmax_workspace_bytes(int64_t M, int64_t K) { return carve_dense(nullptr, M, K, true).bytes; }
+size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K) { return carve_dense(nullptr, M, N, K, false).bytes; }
+size_t argmax_workspace_bytes(int64_t M, int64_t K) { return carve_dense(nullptr, M, 0, K, true).bytes; }
 
 int launch_gemm_w4a16(const uint16_t* X, int64_t M, const nvfp4_tensor_t& W, uint16_t* Y, void* ws,
                       cudaStream_t stream) {
   const int64_t K = W.K, N = W.rows;
-  const DenseWs w = carve_dense(ws, M, K, false);
+  const DenseWs w = carve_dense(ws, M, N, K, false);
   const int nt = static_cast<int>(ceil_div(M < GV_MCHUNK ? M : GV_MCHUNK, 8));
   int rc = prep_dense(X, M, K, nt, w, stream);
   if (rc != NVFP4_OK) return rc;
   const int64_t n_it = K / GV_KIT;
   const int64_t row_tiles = ceil_div(N, GV_ROWS), chunks = ceil_div(M, GV_MCHUNK);
+  if (K % 256 == 0) {
+    // TMA-fed kernel: codes and scales stream through a shared-memory ring
+    CUtensorMap mc, ms;
+    rc = make_tmap_2d_u8(&mc, W.codes, K / 2, N, K / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != NVFP4_OK) return rc;
+    rc = make_tmap_2d_u8(&ms, W.scales, K / 16, N, K / 16, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc != NVFP4_OK) return rc;
+    TmaSkinnyParams q{};
+    q.s_t = W.s_t;
+    q.K = K;
+    q.n_rows = N;
+    q.xfrag = w.xfrag;
+    q.pexp = w.pexp;
+    q.M = M;
+    q.split = tma_split(row_tiles * chunks, n_it / 2);
+    q.Y = Y;
+    q.status = device_status_ptr();
+    q.partials = w.partials;
+    q.counters = w.tile_counters;
+    dim3 grid(static_cast<unsigned>(q.split), static_cast<unsigned>(row_tiles), static_cast<unsigned>(chunks));
+    switch (nt) {
+      case 1: return launch_tma_plain_nt<1>(q, mc, ms, grid, stream);
+      case 2: return launch_tma_plain_nt<2>(q, mc, ms, grid, stream);
+      case 3: return launch_tma_plain_nt<3>(q, mc, ms, grid, stream);
+      default: return launch_tma_plain_nt<4>(q, mc, ms, grid, stream);
+    }
+  }
   SkinnyParams p{};
   p.codes = W.codes;
   p.scales = W.scales;
@@ -107,7 +182,7 @@ int launch_gemm_w4a16(const uint16_t* X, int64_t M, const nvfp4_tensor_t& W, uin
 int launch_gather_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, const int32_t* idx,
                          int64_t n_idx, int32_t* out_ids, float* out_logit, void* ws, cudaStream_t stream) {
   const int64_t K = W.K;
-  const DenseWs w = carve_dense(ws, M, K, true);
+  const DenseWs w = carve_dense(ws, M, 0, K, true);
   // keys and the completion counter start at zero on every call
   if (cudaMemsetAsync(w.keys, 0, reinterpret_cast<char*>(w.pexp) - reinterpret_cast<char*>(w.keys), stream) !=
       cudaSuccess)

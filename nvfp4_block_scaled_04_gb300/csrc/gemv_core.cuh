@@ -50,7 +50,7 @@ inline size_t xfrag_bytes(int64_t chunks, int64_t K) {
 //   out_row index of the row in chunk order (chunk = out_row / 32)
 // Writes p (the power-of-two shift) to pexp[out_row]. One CTA per row.
 NVFP4_DEV void xprep_row(const uint16_t* src, int64_t K, int64_t out_row, uint4* xfrag, int* pexp) {
-  __shared__ float red[GV_THREADS / 32];
+  __shared__ float red[32];
   const int tid = threadIdx.x;
   const int64_t n8 = K / 8;
   float amax = 0.f;
@@ -99,6 +99,64 @@ NVFP4_DEV void xprep_row(const uint16_t* src, int64_t K, int64_t out_row, uint4*
     const int rem = static_cast<int>(q % 16);
     const int t = rem / 4, w = rem % 4;
     xfrag[xfrag_unit(chunk, n_it, it, nt, w, g * 4 + t)] = o;
+  }
+}
+
+// Single-pass version of xprep_row for K <= 8 * 4 * blockDim.x: every thread
+// keeps its (up to four) 16-byte chunks in registers between the amax and the
+// conversion, so the row is read from memory once.
+template <int CHUNKS>
+NVFP4_DEV void xprep_row_regs(const uint16_t* src, int64_t K, int64_t out_row, uint4* xfrag, int* pexp) {
+  __shared__ float red[32];
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int64_t n8 = K / 8;
+  uint4 v[CHUNKS];
+  float amax = 0.f;
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c) {
+    const int64_t q = tid + static_cast<int64_t>(c) * nthr;
+    v[c] = make_uint4(0, 0, 0, 0);
+    if (src != nullptr && q < n8) v[c] = __ldg(reinterpret_cast<const uint4*>(src) + q);
+    const uint32_t w4[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] & 0xFFFFu)));
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] >> 16)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  __syncthreads();
+  if (tid < 32) {
+    float r = tid < nthr / 32 ? red[tid] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = fmaxf(r, __shfl_xor_sync(0xffffffffu, r, o));
+    if (tid == 0) red[0] = r;
+  }
+  __syncthreads();
+  amax = red[0];
+  int p = 0;
+  if (amax > 0.f) p = min(max(ilogbf(amax) - 14, -100), 113);
+  const float mul = ldexpf(1.0f, -p);
+  if (tid == 0) pexp[out_row] = p;
+  const int64_t chunk = out_row / GV_MCHUNK;
+  const int nt = static_cast<int>((out_row % GV_MCHUNK) / 8);
+  const int g = static_cast<int>(out_row % 8);
+  const int64_t n_it = K / GV_KIT;
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c) {
+    const int64_t q = tid + static_cast<int64_t>(c) * nthr;
+    if (q < n8) {
+      uint4 o;
+      o.x = f32x2_to_f16x2(bf16_bits_to_f32(v[c].x & 0xFFFFu) * mul, bf16_bits_to_f32(v[c].x >> 16) * mul);
+      o.y = f32x2_to_f16x2(bf16_bits_to_f32(v[c].y & 0xFFFFu) * mul, bf16_bits_to_f32(v[c].y >> 16) * mul);
+      o.z = f32x2_to_f16x2(bf16_bits_to_f32(v[c].z & 0xFFFFu) * mul, bf16_bits_to_f32(v[c].z >> 16) * mul);
+      o.w = f32x2_to_f16x2(bf16_bits_to_f32(v[c].w & 0xFFFFu) * mul, bf16_bits_to_f32(v[c].w >> 16) * mul);
+      const int64_t it = q / 16;
+      const int rem = static_cast<int>(q % 16);
+      xfrag[xfrag_unit(chunk, n_it, it, nt, rem % 4, g * 4 + rem / 4)] = o;
+    }
   }
 }
 

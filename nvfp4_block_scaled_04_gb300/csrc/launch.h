@@ -2,6 +2,7 @@
 // (api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,26 +16,55 @@ inline int from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4
 int sm_count();
 
 // Launch `kernel` with a thread-block cluster of `cluster_x` CTAs along x
-// (plain launch when cluster_x == 1).
+// (plain launch when cluster_x == 1) and, with `pdl`, programmatic stream
+// serialisation: the kernel may start while the previous kernel on the
+// stream finishes, and must `griddepcontrol.wait` before reading its output.
 template <typename Kernel, typename... Args>
-int launch_cluster(Kernel kernel, dim3 grid, dim3 block, size_t smem, int cluster_x, cudaStream_t stream,
-                   Args... args) {
+int launch_ex(Kernel kernel, dim3 grid, dim3 block, size_t smem, int cluster_x, bool pdl, cudaStream_t stream,
+              Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
   if (cluster_x > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_x);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
   }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
   return from_cuda(cudaLaunchKernelEx(&cfg, kernel, args...));
 }
+
+template <typename Kernel, typename... Args>
+int launch_cluster(Kernel kernel, dim3 grid, dim3 block, size_t smem, int cluster_x, cudaStream_t stream,
+                   Args... args) {
+  return launch_ex(kernel, grid, block, smem, cluster_x, false, stream, args...);
+}
+
+// Raise a kernel's dynamic shared memory limit (once per kernel and device).
+int ensure_smem_impl(const void* func, int bytes);
+template <typename Kernel>
+int ensure_smem(Kernel kernel, int bytes) {
+  return ensure_smem_impl(reinterpret_cast<const void*>(kernel), bytes);
+}
+
+// ---- tma_host.cu: 2-D uint8 tensor map (inner dimension contiguous).
+int make_tmap_2d_u8(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t row_stride,
+                    int box_inner, int box_outer, int swizzle);
+
+// ---- gemm_w4a4.cu: device address of the status word bounded waits write.
+int* device_status_ptr();
 
 // ---- quantize.cu
 int launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
@@ -44,7 +74,7 @@ int launch_prepack_scales(const uint8_t* src, int64_t batch, int64_t rows, int64
 size_t quantize_workspace_bytes();
 
 // ---- gemv.cu
-size_t w4a16_workspace_bytes(int64_t M, int64_t K);
+size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K);
 size_t argmax_workspace_bytes(int64_t M, int64_t K);
 int launch_gemm_w4a16(const uint16_t* X, int64_t M, const nvfp4_tensor_t& W, uint16_t* Y, void* ws,
                       cudaStream_t stream);

@@ -10,7 +10,7 @@
 //
 // Properties a user relies on:
 //   - The array below is part of the library image: every GPU that loads the
-//     library holds it (2 MiB + 4 KiB) until the process exits.
+//     library holds it (8 MiB) until the process exits.
 //   - The host never dereferences `g_noalloc_scratch`; in host code that name
 //     is only a stand-in. Its device address is looked up once per device
 //     with cudaGetSymbolAddress, on the first call made while that device is
@@ -32,7 +32,7 @@ namespace {
 
 constexpr int64_t kNoallocMaxM = 32;
 constexpr int64_t kNoallocMaxK = 32768;
-constexpr size_t kNoallocBytes = (2u << 20) + (4u << 10);
+constexpr size_t kNoallocBytes = 8u << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
 
@@ -66,7 +66,7 @@ extern "C" int nvfp4_gemm_w4a16_noalloc(const void* X, int64_t M, nvfp4_tensor_t
       W.scale_layout != NVFP4_SCALES_ROWMAJOR)
     return NVFP4_ERR_INVALID_ARG;
   if (W.K % 128 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  if (M > kNoallocMaxM || W.K > kNoallocMaxK || w4a16_workspace_bytes(M, W.K) > kNoallocBytes)
+  if (M > kNoallocMaxM || W.K > kNoallocMaxK || w4a16_workspace_bytes(M, W.rows, W.K) > kNoallocBytes)
     return NVFP4_ERR_SCRATCH_LIMIT;
   if (!aligned16(X) || !aligned16(W.codes) || !aligned16(Y)) return NVFP4_ERR_MISALIGNED;
   if (W.rows == 0) return NVFP4_OK;
