@@ -43,17 +43,23 @@ int* device_status_ptr() {
 
 namespace {
 
-constexpr int BM = 128, BN = 128;
-constexpr int BK = 256;                // K elements per stage (128 bytes of codes)
-constexpr int STAGES = 3;
-constexpr int THREADS = 192;
-constexpr int TILE_BYTES = 128 * 128;  // one 128-row x 128-byte code tile
-constexpr int SF_BYTES = 4 * 512;      // four scale atoms per stage
-constexpr int STAGE_BYTES = 2 * TILE_BYTES + 2 * SF_BYTES;
-constexpr int TMEM_COLS = 256;         // 128 accumulator + 3 x 32 scale columns
-constexpr int SF_TMEM_BASE = 128;
+// Tile: 128 rows of A x 256 rows of W per MMA tile, 256 K-elements per stage.
+constexpr int BM = 128, BN = 256;
+constexpr int BK = 256;                     // K elements per stage (128 bytes of codes per row)
+constexpr int STAGES = 4;
+constexpr int EPI_WARPS = 8;                // two per TMEM lane quarter, one per 128-column half
+constexpr int EPI_WARP0 = 3;                // warps 0, 2 produce (even / odd stages), warp 1 issues MMAs
+constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
+constexpr int A_BYTES = BM * 128;           // 16 KB
+constexpr int B_BYTES = BN * 128;           // 32 KB
+constexpr int SFA_BYTES = 4 * 512;          // 4 scale atoms (128 rows x 64 K each)
+constexpr int SFB_BYTES = 2 * 4 * 512;      // 2 row halves x 4 atoms
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;   // 54 KB
+constexpr int TMEM_COLS = 512;              // 256 accumulator + 4 stages x (16 + 32) scale columns
+constexpr int SF_TMEM_BASE = 256;
+constexpr int SF_COLS_PER_STAGE = 48;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr int BAND = 32;               // m-tiles that share one sweep over the W tiles
+constexpr int BAND = 32;                    // m-tiles that share one sweep over the W tiles
 
 // Instruction descriptor: kind::mxf4nvf4, A and B E2M1 (1), both K-major,
 // N>>3 at bit 17, UE4M3 scales (bit 23 = 0), M>>4 at bit 24.
@@ -91,8 +97,8 @@ NVFP4_DEV void tc_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+NVFP4_DEV void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 struct W4A4Params {
   const uint8_t* sfa;   // MMA-layout scales of A
@@ -104,38 +110,48 @@ struct W4A4Params {
   int m_tiles, n_tiles;
 };
 
-__global__ void __launch_bounds__(THREADS, 2)
+// tile index -> (m_tile, n_tile): bands of BAND m-tiles sweep all n-tiles,
+// m fastest, so the CTAs working at one time share A and W tiles in L2
+NVFP4_DEV void tile_coords(int tile, const W4A4Params& p, int& m_tile, int& n_tile) {
+  const int band = tile / (BAND * p.n_tiles);
+  const int band_m0 = band * BAND;
+  const int band_h = min(BAND, p.m_tiles - band_m0);
+  const int within = tile - band * BAND * p.n_tiles;
+  m_tile = band_m0 + within % band_h;
+  n_tile = within / band_h;
+}
+
+// Persistent: CTA c computes tiles c, c + gridDim.x, ...
+//   warps 0, 2  TMA producers over the whole tile sequence (one continuous
+//               ring; warp 0 fills the even stages, warp 2 the odd ones: one
+//               issuing thread cannot keep an SM's TMA ingress busy)
+//   warp 1      TMEM allocation; lane 0 issues scale copies and MMAs
+//   warps 3..10 epilogue: drain the 128 x 256 fp32 accumulator (warp w reads
+//               lane quarter w % 4, column half (w - 3) / 4) into packed bf16
+//               registers, release the accumulator, then store
+__global__ void __launch_bounds__(THREADS, 1)
     gemm_w4a4_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                      const W4A4Params p) {
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte alignment for the 128B-swizzled tiles
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
   const uint32_t bar_base = base + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES);
-  // bars[0..S) full, [S..2S) empty, [2S] accumulator ready
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 2);
+  // bars: [0, S) full, [S, 2S) empty, 2S accumulator full, 2S+1 accumulator empty
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 3);
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
-  const uint32_t acc_bar = bar_base + 8u * (2 * STAGES);
+  const uint32_t accf_bar = bar_base + 8u * (2 * STAGES);
+  const uint32_t acce_bar = bar_base + 8u * (2 * STAGES + 1);
   auto stage_a = [&](int s) { return base + s * STAGE_BYTES; };
-  auto stage_b = [&](int s) { return base + s * STAGE_BYTES + TILE_BYTES; };
-  auto stage_sfa = [&](int s) { return base + s * STAGE_BYTES + 2 * TILE_BYTES; };
-  auto stage_sfb = [&](int s) { return base + s * STAGE_BYTES + 2 * TILE_BYTES + SF_BYTES; };
+  auto stage_b = [&](int s) { return base + s * STAGE_BYTES + A_BYTES; };
+  auto stage_sfa = [&](int s) { return base + s * STAGE_BYTES + A_BYTES + B_BYTES; };
+  auto stage_sfb = [&](int s) { return base + s * STAGE_BYTES + A_BYTES + B_BYTES + SFA_BYTES; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // tile of this CTA: bands of BAND m-tiles sweep all n-tiles, m fastest
-  const int b = blockIdx.x;
-  const int band = b / (BAND * p.n_tiles);
-  const int band_m0 = band * BAND;
-  const int band_h = min(BAND, p.m_tiles - band_m0);
-  const int within = b - band * BAND * p.n_tiles;
-  const int m_tile = band_m0 + within % band_h;
-  const int n_tile = within / band_h;
-  const int m0 = m_tile * BM, n0 = n_tile * BN;
+  const int n_tiles_total = p.m_tiles * p.n_tiles;
   const int n_k = (p.K + BK - 1) / BK;
   const int k_atoms_total = p.K / 64;
   const int64_t sf_row_stride = static_cast<int64_t>(k_atoms_total) * 512;   // bytes per 128-row scale strip
@@ -145,7 +161,8 @@ __global__ void __launch_bounds__(THREADS, 2)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    mbar_init(acc_bar, 1);
+    mbar_init(accf_bar, 1);
+    mbar_init(acce_bar, EPI_WARPS);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_a) : "memory");
@@ -162,90 +179,128 @@ __global__ void __launch_bounds__(THREADS, 2)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  int issued = 0;       // stages whose loads the producer issued
-  bool mma_started = false;
+  int next_it = 0;             // producer: one past the last stage index this thread issued
+  int mma_tiles = 0;           // MMA: tiles whose accumulation was issued
+  const int prod = warp == 0 ? 0 : (warp == 2 ? 1 : -1);
 
-  if (warp == 0) {
+  if (prod >= 0) {
     if (lane == 0) {
-      for (int ks = 0; ks < n_k; ++ks) {
-        const int s = ks % STAGES;
-        if (ks >= STAGES && !mbar_wait_bounded(empty_bar(s), ((ks / STAGES) - 1) & 1, abort_flag, &g_device_status)) break;
-        const int atoms = min(4, k_atoms_total - 4 * ks);
-        const uint32_t sf_bytes = static_cast<uint32_t>(atoms) * 512u;
-        mbar_arrive_expect_tx(full_bar(s), 2u * TILE_BYTES + 2u * sf_bytes);
-        tma_load_2d(stage_a(s), &map_a, ks * 128, m0, full_bar(s));
-        tma_load_2d(stage_b(s), &map_b, ks * 128, n0, full_bar(s));
-        bulk_load(stage_sfa(s), p.sfa + m_tile * sf_row_stride + static_cast<int64_t>(ks) * SF_BYTES, sf_bytes,
-                  full_bar(s));
-        bulk_load(stage_sfb(s), p.sfb + n_tile * sf_row_stride + static_cast<int64_t>(ks) * SF_BYTES, sf_bytes,
-                  full_bar(s));
-        ++issued;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < n_tiles_total && !*abort_flag; tile += gridDim.x) {
+        int m_tile, n_tile;
+        tile_coords(tile, p, m_tile, n_tile);
+        bool ok = true;
+        for (int ks = 0; ks < n_k; ++ks, ++it) {
+          if ((it & 1) != prod) continue;
+          const int s = it % STAGES;
+          if (it >= STAGES &&
+              !mbar_wait_bounded(empty_bar(s), ((it / STAGES) - 1) & 1, abort_flag, &g_device_status)) {
+            ok = false;
+            break;
+          }
+          const int atoms = min(4, k_atoms_total - 4 * ks);
+          const uint32_t sf_bytes = static_cast<uint32_t>(atoms) * 512u;
+          mbar_arrive_expect_tx(full_bar(s), A_BYTES + B_BYTES + 3u * sf_bytes);
+          tma_load_2d(stage_a(s), &map_a, ks * 128, m_tile * BM, full_bar(s));
+          tma_load_2d(stage_b(s), &map_b, ks * 128, n_tile * BN, full_bar(s));
+          bulk_load(stage_sfa(s), p.sfa + m_tile * sf_row_stride + static_cast<int64_t>(ks) * 2048, sf_bytes,
+                    full_bar(s));
+          bulk_load(stage_sfb(s), p.sfb + (2 * n_tile) * sf_row_stride + static_cast<int64_t>(ks) * 2048,
+                    sf_bytes, full_bar(s));
+          // the second 128-row half of a ragged last W tile has no scale atoms of its
+          // own (the scale buffer is padded to 128 rows): reuse the first half's,
+          // those output columns are never stored
+          const int rt_hi = min(2 * n_tile + 1, (p.N + 127) / 128 - 1);
+          bulk_load(stage_sfb(s) + 2048, p.sfb + rt_hi * sf_row_stride + static_cast<int64_t>(ks) * 2048, sf_bytes,
+                    full_bar(s));
+          next_it = it + 1;
+        }
+        if (!ok) break;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int ks = 0; ks < n_k; ++ks) {
-        const int s = ks % STAGES;
-        if (!mbar_wait_bounded(full_bar(s), (ks / STAGES) & 1, abort_flag, &g_device_status)) break;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < n_tiles_total && !*abort_flag; tile += gridDim.x) {
+        // the epilogue must have drained the previous tile's accumulator
+        if (mma_tiles > 0 && !mbar_wait_bounded(acce_bar, (mma_tiles - 1) & 1, abort_flag, &g_device_status)) break;
         tc_fence_after();
-        const int atoms = min(4, k_atoms_total - 4 * ks);
-        const uint32_t sf_col = tmem + SF_TMEM_BASE + s * 32;
-        for (int k = 0; k < atoms; ++k) {
-          tc_cp_sf(sf_col + 4 * k, smem_desc(stage_sfa(s) + 512 * k, 128, 128, 0));
-          tc_cp_sf(sf_col + 16 + 4 * k, smem_desc(stage_sfb(s) + 512 * k, 128, 128, 0));
+        bool ok = true;
+        for (int ks = 0; ks < n_k; ++ks, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait_bounded(full_bar(s), (it / STAGES) & 1, abort_flag, &g_device_status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int atoms = min(4, k_atoms_total - 4 * ks);
+          const uint32_t sf_col = tmem + SF_TMEM_BASE + s * SF_COLS_PER_STAGE;
+          for (int k = 0; k < atoms; ++k) {
+            tc_cp_sf(sf_col + 4 * k, smem_desc(stage_sfa(s) + 512 * k, 128, 128, 0));
+            tc_cp_sf(sf_col + 16 + 8 * k, smem_desc(stage_sfb(s) + 512 * k, 128, 128, 0));
+            tc_cp_sf(sf_col + 16 + 8 * k + 4, smem_desc(stage_sfb(s) + 2048 + 512 * k, 128, 128, 0));
+          }
+          for (int k = 0; k < atoms; ++k) {
+            const uint64_t adesc = smem_desc(stage_a(s) + 32 * k, 16, 1024, 2);
+            const uint64_t bdesc = smem_desc(stage_b(s) + 32 * k, 16, 1024, 2);
+            tc_mma_mxf4nvf4(tmem, adesc, bdesc, IDESC, sf_col + 4 * k, sf_col + 16 + 8 * k,
+                            (ks > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(empty_bar(s));
         }
-        for (int k = 0; k < atoms; ++k) {
-          const uint64_t adesc = smem_desc(stage_a(s) + 32 * k, 16, 1024, 2);
-          const uint64_t bdesc = smem_desc(stage_b(s) + 32 * k, 16, 1024, 2);
-          tc_mma_mxf4nvf4(tmem, adesc, bdesc, IDESC, sf_col + 4 * k, sf_col + 16 + 4 * k,
-                          (ks > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_started = true;
-        tc_commit(empty_bar(s));
+        if (!ok) break;
+        tc_commit(accf_bar);
+        ++mma_tiles;
       }
-      tc_commit(acc_bar);
     }
   } else {
-    // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, one output row per thread
     const int quarter = warp & 3;
-    const int row = m0 + quarter * 32 + lane;
-    if (mbar_wait_bounded(acc_bar, 0, abort_flag, &g_device_status)) {
+    const int half = (warp - EPI_WARP0) >> 2;
+    const float scale = p.st_a[0] * p.st_b[0];
+    int done = 0;
+    for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x, ++done) {
+      int m_tile, n_tile;
+      tile_coords(tile, p, m_tile, n_tile);
+      if (!mbar_wait_bounded(accf_bar, done & 1, abort_flag, &g_device_status)) break;
       tc_fence_after();
-      const float scale = p.st_a[0] * p.st_b[0];
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tc_ld_32cols(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 32u * c, r);
-        const int col0 = n0 + 32 * c;
-        if (row < p.M && col0 < p.N) {
-          uint16_t* dst = p.Y + static_cast<int64_t>(row) * p.N + col0;
-          if (col0 + 32 <= p.N) {
+      uint32_t packed[64];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 v;
-              v.x = f32x2_to_bf16x2(__uint_as_float(r[8 * q + 0]) * scale, __uint_as_float(r[8 * q + 1]) * scale);
-              v.y = f32x2_to_bf16x2(__uint_as_float(r[8 * q + 2]) * scale, __uint_as_float(r[8 * q + 3]) * scale);
-              v.z = f32x2_to_bf16x2(__uint_as_float(r[8 * q + 4]) * scale, __uint_as_float(r[8 * q + 5]) * scale);
-              v.w = f32x2_to_bf16x2(__uint_as_float(r[8 * q + 6]) * scale, __uint_as_float(r[8 * q + 7]) * scale);
-              reinterpret_cast<uint4*>(dst)[q] = v;
-            }
-          } else {
-            for (int j = 0; j < p.N - col0; ++j)
-              dst[j] = static_cast<uint16_t>(f32_to_bf16_bits(__uint_as_float(r[j]) * scale));
-          }
-        }
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc_ld_32cols(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(half * 128 + 32 * c), r);
+        tc_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          packed[16 * c + q] = f32x2_to_bf16x2(__uint_as_float(r[2 * q]) * scale, __uint_as_float(r[2 * q + 1]) * scale);
+      }
+      // the accumulator is free for the next tile's MMAs
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar);
+      const int row = m_tile * BM + quarter * 32 + lane;
+      const int col0 = n_tile * BN + half * 128;
+      if (row < p.M && col0 < p.N) {
+        uint16_t* dst = p.Y + static_cast<int64_t>(row) * p.N + col0;
+        const int nq = (p.N - col0) >= 128 ? 16 : (p.N - col0) / 8;   // 16-byte pieces in range
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          if (q < nq)
+            reinterpret_cast<uint4*>(dst)[q] =
+                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
       }
     }
   }
 
-  // Unwind. If a wait gave up, let the copies and MMAs already issued finish
+  // Unwind. After a give-up, let the copies and MMAs already issued land
   // (bounded) before the shared and tensor memory they target go away.
-  if (warp == 0 && lane == 0 && *abort_flag) {
-    for (int ks = 0; ks < issued; ++ks)
-      mbar_wait_bounded(full_bar(ks % STAGES), (ks / STAGES) & 1, nullptr, &g_device_status, 100000000ull);
+  if (prod >= 0 && lane == 0 && *abort_flag) {
+    // the stages of this producer that may still be in flight: its last ones
+    for (int it = next_it - 1; it >= 0 && it >= next_it - 2 * STAGES; --it)
+      if ((it & 1) == prod)
+        mbar_wait_bounded(full_bar(it % STAGES), (it / STAGES) & 1, nullptr, &g_device_status, 100000000ull);
   }
-  if (warp == 1 && lane == 0 && *abort_flag && mma_started) {
-    mbar_wait_bounded(acc_bar, 0, nullptr, &g_device_status, 100000000ull);
+  if (warp == 1 && lane == 0 && *abort_flag && mma_tiles > 0) {
+    mbar_wait_bounded(accf_bar, (mma_tiles - 1) & 1, nullptr, &g_device_status, 100000000ull);
   }
   tc_fence_before();
   __syncthreads();
@@ -281,8 +336,8 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns) {
 }
 
 // 2-D map over packed codes [rows][K/2] bytes, 128 x 128-byte boxes, 128B swizzle.
-int make_code_map(CUtensorMap* map, const uint8_t* codes, int64_t rows, int64_t K) {
-  return make_tmap_2d_u8(map, codes, K / 2, rows, K / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+int make_code_map(CUtensorMap* map, const uint8_t* codes, int64_t rows, int64_t K, int box_rows) {
+  return make_tmap_2d_u8(map, codes, K / 2, rows, K / 2, 128, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 constexpr size_t kAlign = 256;
@@ -316,18 +371,13 @@ int launch_gemm_w4a4(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t*
     sfb = dst;
   }
   CUtensorMap map_a, map_b;
-  int rc = make_code_map(&map_a, A.codes, M, K);
+  int rc = make_code_map(&map_a, A.codes, M, K, BM);
   if (rc != NVFP4_OK) return rc;
-  rc = make_code_map(&map_b, W.codes, N, K);
+  rc = make_code_map(&map_b, W.codes, N, K, BN);
   if (rc != NVFP4_OK) return rc;
 
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(gemm_w4a4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-        cudaSuccess)
-      return NVFP4_ERR_CUDA;
-    attr_set = true;
-  }
+  rc = ensure_smem(gemm_w4a4_kernel, SMEM_BYTES);
+  if (rc != NVFP4_OK) return rc;
   W4A4Params p{};
   p.sfa = sfa;
   p.sfb = sfb;
@@ -339,7 +389,8 @@ int launch_gemm_w4a4(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t*
   p.K = static_cast<int>(K);
   p.m_tiles = static_cast<int>(ceil_div(M, BM));
   p.n_tiles = static_cast<int>(ceil_div(N, BN));
-  const unsigned grid = static_cast<unsigned>(p.m_tiles) * static_cast<unsigned>(p.n_tiles);
+  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+  const unsigned grid = static_cast<unsigned>(tiles < sm_count() ? tiles : sm_count());
   gemm_w4a4_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(map_a, map_b, p);
   return from_cuda(cudaGetLastError());
 }
