@@ -6,15 +6,18 @@
 // the per-16 E4M3 scales and accumulates in fp32 in tensor memory; the
 // epilogue applies the two fp32 tensor scales and rounds to bf16.
 //
-// One CTA computes a 128 x 128 output tile:
-//   warp 0       TMA producer: A and W code tiles (128 rows x 128 bytes, 128B
-//                swizzle) and their block scales (already in the MMA scale
-//                layout: one 512-byte atom per 128 rows x 64 K) into a
-//                3-stage shared-memory ring
-//   warp 1       allocates tensor memory; one lane copies the stage's scale
-//                atoms into tensor memory (tcgen05.cp) and issues
-//                tcgen05.mma.kind::mxf4nvf4 (M=128, N=128, K=64 each)
-//   warps 2..5   epilogue: tcgen05.ld of the fp32 accumulator, scale, bf16
+// A persistent CTA per SM computes 128 x 256 output tiles. Each stage of a
+// 4-deep shared-memory ring holds 256 K of the A and W code tiles (128B
+// swizzle) and their block scales, already in the MMA scale layout (one
+// 512-byte atom per 128 rows x 64 K).
+//
+// The block scales reach tensor memory through registers: four scale warps,
+// one per tensor-memory lane quarter, read each stage's atoms from shared
+// memory and write them with tcgen05.st. Copying them with tcgen05.cp costs
+// about as much tensor-pipe time per instruction as a 128 x 256 x 64 MMA
+// (measured on sm_103a: ~100 vs ~128 clocks), and one stage needs twelve
+// atoms, so on the tensor pipe the copies took longer than the MMAs they
+// fed; tcgen05.st from other warps runs beside the MMAs without slowing them.
 // Every mbarrier wait is bounded; a wait that gives up records
 // NVFP4_ERR_TIMEOUT in a device status word and the CTA unwinds, frees its
 // tensor memory and exits.
@@ -49,7 +52,9 @@ constexpr int BK = 256;                     // K elements per stage (128 bytes o
 constexpr int STAGES = 4;
 constexpr int EPI_WARPS = 8;                // two per TMEM lane quarter, one per 128-column half
 constexpr int EPI_WARP0 = 3;                // warps 0, 2 produce (even / odd stages), warp 1 issues MMAs
-constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
+constexpr int SF_WARPS = 4;                 // one per TMEM lane quarter
+constexpr int SF_WARP0 = EPI_WARP0 + EPI_WARPS;
+constexpr int THREADS = (SF_WARP0 + SF_WARPS) * 32;
 constexpr int A_BYTES = BM * 128;           // 16 KB
 constexpr int B_BYTES = BN * 128;           // 32 KB
 constexpr int SFA_BYTES = 4 * 512;          // 4 scale atoms (128 rows x 64 K each)
@@ -59,6 +64,7 @@ constexpr int TMEM_COLS = 512;              // 256 accumulator + 4 stages x (16 
 constexpr int SF_TMEM_BASE = 256;
 constexpr int SF_COLS_PER_STAGE = 48;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+static_assert((3 * STAGES + 4) * 8 <= 256, "barrier area");
 constexpr int BAND = 32;                    // m-tiles that share one sweep over the W tiles
 
 // Instruction descriptor: kind::mxf4nvf4, A and B E2M1 (1), both K-major,
@@ -68,8 +74,21 @@ constexpr uint32_t IDESC = (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | 
 NVFP4_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 NVFP4_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
-NVFP4_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+// 16 consecutive 32-bit tensor-memory columns of this warp's 32 lanes
+NVFP4_DEV void tc_st_16cols(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+NVFP4_DEV void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+NVFP4_DEV uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
 }
 
 NVFP4_DEV void tc_mma_mxf4nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
@@ -125,10 +144,14 @@ NVFP4_DEV void tile_coords(int tile, const W4A4Params& p, int& m_tile, int& n_ti
 //   warps 0, 2  TMA producers over the whole tile sequence (one continuous
 //               ring; warp 0 fills the even stages, warp 2 the odd ones: one
 //               issuing thread cannot keep an SM's TMA ingress busy)
-//   warp 1      TMEM allocation; lane 0 issues scale copies and MMAs
+//   warp 1      TMEM allocation; lane 0 issues the MMAs
 //   warps 3..10 epilogue: drain the 128 x 256 fp32 accumulator (warp w reads
 //               lane quarter w % 4, column half (w - 3) / 4) into packed bf16
 //               registers, release the accumulator, then store
+//   warps 11..14 scale warps: copy each stage's scale atoms from shared
+//               memory into that stage's tensor-memory scale columns
+// A warp may touch only the tensor-memory lane quarter warp % 4; every branch
+// that ends in a .sync.aligned tcgen05 instruction is taken warp-uniformly.
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_w4a4_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                      const W4A4Params p) {
@@ -138,13 +161,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* base_ptr = smem_raw + (base - raw);
   const uint32_t bar_base = base + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES);
-  // bars: [0, S) full, [S, 2S) empty, 2S accumulator full, 2S+1 accumulator empty
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 3);
+  // bars: [0, S) full, [S, 2S) empty, [2S, 3S) scales in tensor memory,
+  // 3S accumulator full, 3S+1 accumulator empty
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * STAGES + 3);
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
-  const uint32_t accf_bar = bar_base + 8u * (2 * STAGES);
-  const uint32_t acce_bar = bar_base + 8u * (2 * STAGES + 1);
+  auto sf_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + s); };
+  const uint32_t accf_bar = bar_base + 8u * (3 * STAGES);
+  const uint32_t acce_bar = bar_base + 8u * (3 * STAGES + 1);
   auto stage_a = [&](int s) { return base + s * STAGE_BYTES; };
   auto stage_b = [&](int s) { return base + s * STAGE_BYTES + A_BYTES; };
   auto stage_sfa = [&](int s) { return base + s * STAGE_BYTES + A_BYTES + B_BYTES; };
@@ -160,6 +185,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(sf_bar(s), SF_WARPS);
     }
     mbar_init(accf_bar, 1);
     mbar_init(acce_bar, EPI_WARPS);
@@ -228,18 +254,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool ok = true;
         for (int ks = 0; ks < n_k; ++ks, ++it) {
           const int s = it % STAGES;
-          if (!mbar_wait_bounded(full_bar(s), (it / STAGES) & 1, abort_flag, &g_device_status)) {
+          // the scale warps arrive only after the stage's copies landed
+          if (!mbar_wait_bounded(sf_bar(s), (it / STAGES) & 1, abort_flag, &g_device_status)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const int atoms = min(4, k_atoms_total - 4 * ks);
           const uint32_t sf_col = tmem + SF_TMEM_BASE + s * SF_COLS_PER_STAGE;
-          for (int k = 0; k < atoms; ++k) {
-            tc_cp_sf(sf_col + 4 * k, smem_desc(stage_sfa(s) + 512 * k, 128, 128, 0));
-            tc_cp_sf(sf_col + 16 + 8 * k, smem_desc(stage_sfb(s) + 512 * k, 128, 128, 0));
-            tc_cp_sf(sf_col + 16 + 8 * k + 4, smem_desc(stage_sfb(s) + 2048 + 512 * k, 128, 128, 0));
-          }
           for (int k = 0; k < atoms; ++k) {
             const uint64_t adesc = smem_desc(stage_a(s) + 32 * k, 16, 1024, 2);
             const uint64_t bdesc = smem_desc(stage_b(s) + 32 * k, 16, 1024, 2);
@@ -253,7 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         ++mma_tiles;
       }
     }
-  } else {
+  } else if (warp < SF_WARP0) {
     const int quarter = warp & 3;
     const int half = (warp - EPI_WARP0) >> 2;
     const float scale = p.st_a[0] * p.st_b[0];
@@ -261,7 +283,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x, ++done) {
       int m_tile, n_tile;
       tile_coords(tile, p, m_tile, n_tile);
-      if (!mbar_wait_bounded(accf_bar, done & 1, abort_flag, &g_device_status)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(accf_bar, done & 1, abort_flag, &g_device_status))) break;
       tc_fence_after();
       uint32_t packed[64];
 #pragma unroll
@@ -288,6 +310,51 @@ __global__ void __launch_bounds__(THREADS, 1)
             reinterpret_cast<uint4*>(dst)[q] =
                 make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
       }
+    }
+  } else {
+    // Scale warps. Stage layout of the scale columns: [4k, 4k + 4) atom k of
+    // A, [16 + 8k, 16 + 8k + 8) atom k of W's two 128-row halves. Lane l of
+    // every lane quarter holds line l of each atom, whose four 32-bit words are
+    // the four K-scales of rows l, l + 32, l + 64, l + 96 (the MMA reads the
+    // word of its own quarter).
+    const uint32_t lane_cols = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + SF_TMEM_BASE;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      bool ok = true;
+      for (int ks = 0; ks < n_k; ++ks, ++it) {
+        const int s = it % STAGES;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_bounded(full_bar(s), (it / STAGES) & 1, abort_flag, &g_device_status))) {
+          ok = false;
+          break;
+        }
+        uint32_t v[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 x = lds128(stage_sfa(s) + 512 * k + 16 * lane);
+          v[4 * k] = x.x, v[4 * k + 1] = x.y, v[4 * k + 2] = x.z, v[4 * k + 3] = x.w;
+        }
+        const uint32_t col = lane_cols + s * SF_COLS_PER_STAGE;
+        tc_st_16cols(col, v);
+#pragma unroll
+        for (int pair = 0; pair < 2; ++pair) {
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint4 x = lds128(stage_sfb(s) + 2048 * h + 512 * (2 * pair + kk) + 16 * lane);
+              const int o = 8 * kk + 4 * h;
+              v[o] = x.x, v[o + 1] = x.y, v[o + 2] = x.z, v[o + 3] = x.w;
+            }
+          tc_st_16cols(col + 16 + 16 * pair, v);
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sf_bar(s));
+      }
+      if (!ok) break;
     }
   }
 
