@@ -13,11 +13,16 @@ namespace {
 // M, up to the n-tile padding of the chunk, become zeros).
 // CTA (0, 0) also zeroes the split-K arrival counters of the GEMV that follows.
 // 1024 threads per row: up to K = 32768 the row is read once, into registers.
+// Launched as a programmatic dependent of whatever kernel precedes it on the
+// stream: it lets its own GEMV launch at once (that GEMV starts streaming its
+// weights) and then waits for the preceding kernel to finish before it
+// touches memory - which may be that kernel's output, or a workspace it uses.
 constexpr int XPREP_THREADS = 1024;
 __global__ void __launch_bounds__(XPREP_THREADS) xprep_dense_kernel(const uint16_t* X, int64_t M, int64_t K,
                                                                      uint4* xfrag, int* pexp,
                                                                      unsigned int* counters, int n_counters) {
   pdl_launch_dependents();
+  pdl_wait();
   if (blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
   const int64_t out_row = static_cast<int64_t>(blockIdx.y) * GV_MCHUNK + blockIdx.x;
@@ -118,9 +123,8 @@ DenseWs carve_dense(void* base, int64_t M, int64_t N, int64_t K, bool argmax) {
 int prep_dense(const uint16_t* X, int64_t M, int64_t K, int nt, const DenseWs& w, cudaStream_t stream) {
   const int64_t chunks = ceil_div(M, GV_MCHUNK);
   dim3 grid(static_cast<unsigned>(8 * nt), static_cast<unsigned>(chunks));
-  xprep_dense_kernel<<<grid, XPREP_THREADS, 0, stream>>>(X, M, K, w.xfrag, w.pexp, w.tile_counters,
-                                                         w.n_tile_counters);
-  return from_cuda(cudaGetLastError());
+  return launch_ex(xprep_dense_kernel, grid, dim3(XPREP_THREADS), 0, 1, true, stream, X, M, K, w.xfrag, w.pexp,
+                   w.tile_counters, w.n_tile_counters);
 }
 
 }  // namespace

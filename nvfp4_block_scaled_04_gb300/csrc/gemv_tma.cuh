@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
     skinny_tma_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
                       const TmaSkinnyParams p) {
   using C = GtCfg<NT>;
+  pdl_launch_dependents();   // the next call's activation prep may queue up now
   constexpr int NCW = GtWarps<MT, KW>::CONSUMERS;
   constexpr int NGR = GtWarps<MT, KW>::GROUPS;
   constexpr int NTHR = GtWarps<MT, KW>::THREADS;
@@ -333,8 +334,14 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
       for (int e = tid; e < rows_in_chunk * GV_ROWS; e += NTHR) {
         const int tok = e / GV_ROWS;
         const int r = e % GV_ROWS;
+        // all S (<= 8) partials in flight at once, summed in split order
+        float x[8];
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) x[qq] = qq < S ? __ldcg(all + (qq * GV_MCHUNK + tok) * GV_ROWS + r) : 0.f;
         float v = 0.f;
-        for (int qq = 0; qq < S; ++qq) v += __ldcg(all + (qq * GV_MCHUNK + tok) * GV_ROWS + r);
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq)
+          if (qq < S) v += x[qq];
         const int64_t n = row_tile * GV_ROWS + r;
         if (n < p.n_rows)
           p.Y[(row_base + tok) * p.n_rows + n] =
