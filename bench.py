@@ -171,6 +171,22 @@ def capture(fn):
     return g
 
 
+_CLEAN = {}
+
+
+def l2_flush(flush):
+    """Write `flush` (larger than L2), then read a clean buffer of the same
+    size: the written lines are evicted (and written back) here, so the timed
+    replay that follows starts from an L2 holding only clean, unrelated data
+    and pays no write-back of the flush."""
+    import torch
+    flush.zero_()
+    clean = _CLEAN.get(flush.numel())
+    if clean is None:
+        clean = _CLEAN[flush.numel()] = torch.zeros(flush.numel() // 4, dtype=torch.float32, device=flush.device)
+    clean.sum()
+
+
 def time_graph(g, reps, warmup=3, flush=None):
     """Mean ms per replay. With `flush`, L2 is flushed before every replay and
     only the replay is timed (the flush keeps the GPU busy while the replay is
@@ -189,7 +205,7 @@ def time_graph(g, reps, warmup=3, flush=None):
         return a.elapsed_time(b) / reps
     total = 0.0
     for _ in range(reps):
-        flush.zero_()
+        l2_flush(flush)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         g.replay()

@@ -104,7 +104,9 @@ typedef struct nvfp4_tensor {
  *   s_t        device fp32: written (COMPUTE) or read (GIVEN)
  *   workspace  device, >= nvfp4_workspace_size(NVFP4_OP_QUANTIZE, ...) bytes
  *              (COMPUTE only; may be NULL for GIVEN); contents are scratch.
- * K must be a multiple of 16. rows == 0 is a no-op (COMPUTE writes s_t = 1). */
+ * K must be a multiple of 16, and rows * ceil(K / 1024) must stay below 2^30
+ * (NVFP4_ERR_UNSUPPORTED_SHAPE otherwise). rows == 0 is a no-op (COMPUTE
+ * writes s_t = 1). */
 int nvfp4_quantize(const void* x, int x_dtype, int64_t rows, int64_t K,
                    uint8_t* codes, uint8_t* scales, float* s_t, int s_t_mode,
                    int scale_layout, void* workspace, size_t workspace_bytes,

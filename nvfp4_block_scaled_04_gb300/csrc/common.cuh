@@ -67,6 +67,21 @@ NVFP4_DEV float e4m3_to_f32(uint32_t c) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));                 // (1+m/8) 2^(e-7)
 }
 
+// Eight fp32 -> eight e2m1 codes, element j in nibble j (round to nearest
+// even, saturating at 6; a negative value that rounds to zero keeps its sign).
+NVFP4_DEV uint32_t f32x8_to_e2m1x8(const float (&v)[8]) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return out;
+}
+
 // Two non-negative fp32 -> packed e2m1 magnitudes (a in the low nibble,
 // b in the high nibble), nearest-even, saturating to 6.
 NVFP4_DEV uint32_t f32x2_to_e2m1x2(float a, float b) {

@@ -41,12 +41,24 @@ NVFP4_DEV void load8<float>(const float* p, float (&v)[8]) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+// Four 8-element loads in flight per thread; the pass walks the tensor from
+// its start to its end, so its last part is what the L2 holds afterwards.
 template <typename T>
 __global__ void __launch_bounds__(Q_THREADS) amax_kernel(const T* x, int64_t n8, unsigned int* out) {
   __shared__ float red[Q_THREADS / 32];
   float m = 0.f;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    float v[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) load8<T>(x + (i + u * stride) * 8, v[u]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[u][e]));
+  }
+  for (; i < n8; i += stride) {
     float v[8];
     load8<T>(x + i * 8, v);
 #pragma unroll
@@ -71,13 +83,78 @@ NVFP4_DEV int64_t mma_scale_offset(int64_t row, int64_t col, int64_t cols4) {
   return tile * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (col & 3);
 }
 
-// Each lane quantises half a block (8 elements); lanes 2i and 2i+1 hold the
-// two halves of one block.
+// Eight codes of one block half, packed: element j in nibble j. The code is
+// RNE_e2m1(fl(x / den)) with the sign of x kept on a zero magnitude; the
+// conversion instruction rounds to nearest even, saturates at 6 and keeps the
+// sign of a negative quotient that rounds to zero. The code depends only on
+// which side of the e2m1 rounding midpoints the quotient lies:
+// q~ = x * RN(1/den) is within ~2^-22 (relative) of fl(x / den), so if
+// q~ (1 - 2^-20) and q~ (1 + 2^-20) give the same codes, no midpoint lies
+// near any of the eight quotients and those are the codes of the exact
+// quotients; otherwise (ties, values at a midpoint's edge) the eight
+// quotients are formed by IEEE division.
+NVFP4_DEV uint32_t e2m1x8(const float* v, float den, float r, bool fast) {
+  if (fast) {
+    float hi[8], lo[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float q = __fmul_rn(v[j], r);
+      hi[j] = __fmul_rn(q, 1.0f + 0x1p-20f);
+      lo[j] = __fmul_rn(q, 1.0f - 0x1p-20f);
+    }
+    const uint32_t a = f32x8_to_e2m1x8(hi), b = f32x8_to_e2m1x8(lo);
+    if (a == b) return a;
+  }
+  float q[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(v[j], den);
+  return f32x8_to_e2m1x8(q);
+}
+
+// 16-byte words of one 16-element block: 2 (bf16) or 4 (fp32).
+template <typename T>
+struct BlockWords {
+  static constexpr int N = static_cast<int>(sizeof(T));
+};
+
+template <typename T>
+NVFP4_DEV void unpack16(const uint4 (&w)[BlockWords<T>::N], float (&v)[16]);
+template <>
+NVFP4_DEV void unpack16<uint16_t>(const uint4 (&w)[2], float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t u[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[8 * i + 2 * e] = bf16_bits_to_f32(u[e] & 0xFFFFu);
+      v[8 * i + 2 * e + 1] = bf16_bits_to_f32(u[e] >> 16);
+    }
+  }
+}
+template <>
+NVFP4_DEV void unpack16<float>(const uint4 (&w)[4], float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[4 * i] = __uint_as_float(w[i].x);
+    v[4 * i + 1] = __uint_as_float(w[i].y);
+    v[4 * i + 2] = __uint_as_float(w[i].z);
+    v[4 * i + 3] = __uint_as_float(w[i].w);
+  }
+}
+
+// One thread quantises BPT blocks of 16 elements, 32 blocks apart in the row:
+// the raw words of all of them are requested before any is converted, so
+// 2 KB per warp are in flight, at up to 48 warps per SM. The block scale is formed once per block; a
+// warp covers 32 * BPT consecutive blocks of a row. Warps take these chunks
+// from the END of the tensor backwards: right after the amax pass, the tail
+// of the input is still in L2.
 template <typename T, int LAYOUT>
-__global__ void __launch_bounds__(Q_THREADS) quantize_kernel(const T* x, int64_t rows, int64_t K,
-                                                              uint8_t* codes, uint8_t* scales,
-                                                              const unsigned int* amax_bits, float* s_t,
-                                                              int mode, int64_t cols4) {
+__global__ void __launch_bounds__(Q_THREADS, 6) quantize_kernel(const T* x, int64_t rows, int64_t K,
+                                                                 uint8_t* codes, uint8_t* scales,
+                                                                 const unsigned int* amax_bits, float* s_t,
+                                                                 int mode, int64_t cols4) {
+  constexpr int NW = BlockWords<T>::N;
+  constexpr int BPT = 4 / NW;   // 2 blocks (bf16) or 1 (fp32) per thread
   float st;
   if (mode == NVFP4_ST_COMPUTE) {
     const float amax = __uint_as_float(*amax_bits);
@@ -87,47 +164,47 @@ __global__ void __launch_bounds__(Q_THREADS) quantize_kernel(const T* x, int64_t
     st = *s_t;
   }
   const float d = __fmul_rn(st, 6.0f);
-  const int64_t halves_per_row = K / 8;
-  const int64_t total = rows * halves_per_row;
+  // chunk indices fit in 32 bits (checked at launch): no 64-bit division here
+  const uint32_t bpr = static_cast<uint32_t>(K / 16);
+  const uint32_t cpr = (bpr + 32 * BPT - 1) / (32 * BPT);
   const int lane = threadIdx.x & 31;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31); base < total;
-       base += stride) {
-    const int64_t h = base + lane;
-    const bool valid = h < total;
-    float v[8];
-    if (valid) {
-      load8<T>(x + h * 8, v);
-    } else {
+  const int warps = static_cast<int>(gridDim.x * (blockDim.x / 32));
+  const int n_chunks = static_cast<int>(rows * cpr);
+  for (int c = n_chunks - 1 - static_cast<int>(blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)); c >= 0;
+       c -= warps) {
+    const uint32_t row32 = static_cast<uint32_t>(c) / cpr;
+    const uint32_t b0 = (static_cast<uint32_t>(c) - row32 * cpr) * (32 * BPT) + lane;
+    const int64_t row = row32;
+    uint4 raw[BPT][NW];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = 0.f;
+    for (int u = 0; u < BPT; ++u) {
+      const uint32_t bi = b0 + 32 * u;
+      const uint4* src = reinterpret_cast<const uint4*>(x + (row * bpr + (bi < bpr ? bi : 0)) * 16);
+#pragma unroll
+      for (int i = 0; i < NW; ++i) raw[u][i] = __ldg(src + i);
     }
-    float am = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(v[e]));
-    const float ab = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-    const uint32_t sc = f32_to_e4m3(__fdiv_rn(ab, d));
-    uint32_t packed = 0;
-    if (sc != 0) {
-      const float den = __fmul_rn(e4m3_to_f32(sc), st);
+    for (int u = 0; u < BPT; ++u) {
+      const uint32_t bi = b0 + 32 * u;
+      if (bi >= bpr) continue;
+      const int64_t blk = row * bpr + bi;
+      float v[16];
+      unpack16<T>(raw[u], v);
+      float ab = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float q0 = __fdiv_rn(v[2 * e], den);
-        const float q1 = __fdiv_rn(v[2 * e + 1], den);
-        uint32_t byte = f32x2_to_e2m1x2(fabsf(q0), fabsf(q1));
-        byte |= (__float_as_uint(v[2 * e]) >> 31) << 3;
-        byte |= (__float_as_uint(v[2 * e + 1]) >> 31) << 7;
-        packed |= byte << (8 * e);
+      for (int e = 0; e < 16; ++e) ab = fmaxf(ab, fabsf(v[e]));
+      const uint32_t sc = f32_to_e4m3(__fdiv_rn(ab, d));
+      uint2 packed = make_uint2(0u, 0u);
+      if (sc != 0) {
+        const float den = __fmul_rn(e4m3_to_f32(sc), st);
+        const float r = __frcp_rn(den);
+        const bool fast = den > 1e-30f && den < 1e30f;
+        packed.x = e2m1x8(v, den, r, fast);
+        packed.y = e2m1x8(v + 8, den, r, fast);
       }
-    }
-    if (valid) {
-      reinterpret_cast<uint32_t*>(codes)[h] = packed;
-      if ((h & 1) == 0) {
-        const int64_t row = h / halves_per_row;
-        const int64_t col = (h % halves_per_row) >> 1;
-        const int64_t off = LAYOUT == NVFP4_SCALES_MMA ? mma_scale_offset(row, col, cols4) : row * (K / 16) + col;
-        scales[off] = static_cast<uint8_t>(sc);
-      }
+      reinterpret_cast<uint2*>(codes)[blk] = packed;
+      const int64_t off = LAYOUT == NVFP4_SCALES_MMA ? mma_scale_offset(row, bi, cols4) : blk;
+      scales[off] = static_cast<uint8_t>(sc);
     }
   }
 }
@@ -179,6 +256,7 @@ int launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t
         amax_kernel<float><<<g, Q_THREADS, 0, stream>>>(static_cast<const float*>(x), n8, amax);
     }
   }
+  if (rows * ((K / 16 + 63) / 64) >= (1LL << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   const int g = grid_for(n8 > 0 ? n8 : 1, Q_THREADS);
 #define NVFP4_Q(T, L)                                                                                  \
   quantize_kernel<T, L><<<g, Q_THREADS, 0, stream>>>(static_cast<const T*>(x), rows, K, codes, scales, \

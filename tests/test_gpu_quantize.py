@@ -101,3 +101,29 @@ def test_full_size_prefill_activations_mma_layout():
     a = synth.prefill_inputs(M=8192)[0]
     q = m.quantize(a.to(DEV), scale_layout=m.SCALES_MMA)
     check(q, O.quantize(a.float().numpy()), 1)
+
+
+def test_values_next_to_rounding_midpoints():
+    """Element quotients a few ulps either side of every e2m1 rounding
+    midpoint (and exactly on it), for many block scales: the code decision
+    there must equal the one the IEEE-divided quotient gives."""
+    m = nv()
+    rng = np.random.default_rng(21)
+    rows, blocks = 256, 32
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], dtype=np.float64)
+    # block scales: E4M3 normals 2^-6 .. 448 (mantissas 1 + j/8)
+    exps = rng.integers(-6, 9, size=(rows, blocks))
+    mans = 1.0 + rng.integers(0, 8, size=(rows, blocks)) / 8.0
+    den = np.minimum(mans * np.exp2(exps), 448.0)
+    x = np.empty((rows, blocks, 16), dtype=np.float32)
+    x[:, :, 0] = (6.0 * den).astype(np.float32)          # the block amax: scale == den exactly (s_t = 1)
+    mid = rng.choice(mids, size=(rows, blocks, 15))
+    k = rng.integers(-4, 5, size=(rows, blocks, 15))
+    q = (mid * (1.0 + k * 2.0 ** -23)).astype(np.float32)
+    x[:, :, 1:] = (q.astype(np.float64) * den[:, :, None]).astype(np.float32)
+    x *= np.where(rng.random(x.shape) < 0.5, -1.0, 1.0).astype(np.float32)
+    x[:, :, 0] = np.abs(x[:, :, 0])
+    x = x.reshape(rows, blocks * 16)
+    for layout in (0, 1):
+        qg = m.quantize(torch.from_numpy(x).to(DEV), s_t=torch.tensor([1.0]), scale_layout=layout)
+        check(qg, O.quantize(x, s_t=np.float32(1.0)), layout)
