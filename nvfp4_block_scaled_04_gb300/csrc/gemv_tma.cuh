@@ -86,6 +86,55 @@ NVFP4_DEV uint4 lds_v4(uint32_t saddr) {
   return v;
 }
 
+// One K-iteration (128 K) of a stage: the warp's MT m-tiles of 16 weight rows
+// (row group grp) against NT n-tiles of 8 tokens; j selects the iteration
+// within the stage (codes at 16-byte chunks 4j..4j+3 of each 128-byte row,
+// scales at bytes 8j..8j+7, activation fragments at j * NT * 2048).
+template <int NT, int MT>
+NVFP4_DEV void gt_mma_iteration(uint32_t stage, int j, int grp, int sw, int t, int lane, float (&acc)[MT][NT][4]) {
+  const uint32_t phys = static_cast<uint32_t>(((4 * j + t) ^ sw) << 4);
+  uint32_t wa[MT][4], wb[MT][4], sa[MT][2], sb[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const int rl = (grp * MT + mt) * 16 + sw;
+    const uint4 ca = lds_v4(stage + rl * 128 + phys);
+    const uint4 cb = lds_v4(stage + (rl + 8) * 128 + phys);
+    wa[mt][0] = ca.x; wa[mt][1] = ca.y; wa[mt][2] = ca.z; wa[mt][3] = ca.w;
+    wb[mt][0] = cb.x; wb[mt][1] = cb.y; wb[mt][2] = cb.z; wb[mt][3] = cb.w;
+    const uint32_t scA = e4m3x2_to_f16x2(lds_u16(stage + GT_CODES + rl * 16 + 8 * j + 2 * t));
+    const uint32_t scB = e4m3x2_to_f16x2(lds_u16(stage + GT_CODES + (rl + 8) * 16 + 8 * j + 2 * t));
+    sa[mt][0] = dup_lo(scA); sa[mt][1] = dup_hi(scA);
+    sb[mt][0] = dup_lo(scB); sb[mt][1] = dup_hi(scB);
+  }
+  const uint32_t xs = stage + GT_CODES + GT_SCALES + j * NT * 2048 + lane * 16;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t A0[MT][4], A1[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      uint32_t fa[4], fb[4];
+      e2m1x8_to_f16x2(wa[mt][w], fa);
+      e2m1x8_to_f16x2(wb[mt][w], fb);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        fa[e] = hmul2(fa[e], sa[mt][w >> 1]);
+        fb[e] = hmul2(fb[e], sb[mt][w >> 1]);
+      }
+      A0[mt][0] = fa[0]; A0[mt][1] = fb[0]; A0[mt][2] = fa[1]; A0[mt][3] = fb[1];
+      A1[mt][0] = fa[2]; A1[mt][1] = fb[2]; A1[mt][2] = fa[3]; A1[mt][3] = fb[3];
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint4 bx = lds_v4(xs + (nt * 4 + w) * 512);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        mma_f16_16816(acc[mt][nt], A0[mt], bx.x, bx.y);
+        mma_f16_16816(acc[mt][nt], A1[mt], bx.z, bx.w);
+      }
+    }
+  }
+}
+
 template <int NT, int MODE, int MT, int KW>
 __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
     skinny_tma_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
@@ -223,47 +272,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
       for (int jj = 0; jj < 3 - KW; ++jj) {
         const int j = KW == 2 ? jk : jj;
         if (it0 + 2LL * st + j < it_end) {
-          const uint32_t phys = static_cast<uint32_t>(((4 * j + t) ^ sw) << 4);
-          uint32_t wa[MT][4], wb[MT][4], sa[MT][2], sb[MT][2];
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const int rl = (grp * MT + mt) * 16 + sw;
-            const uint4 ca = lds_v4(stage + rl * 128 + phys);
-            const uint4 cb = lds_v4(stage + (rl + 8) * 128 + phys);
-            wa[mt][0] = ca.x; wa[mt][1] = ca.y; wa[mt][2] = ca.z; wa[mt][3] = ca.w;
-            wb[mt][0] = cb.x; wb[mt][1] = cb.y; wb[mt][2] = cb.z; wb[mt][3] = cb.w;
-            const uint32_t scA = e4m3x2_to_f16x2(lds_u16(stage + GT_CODES + rl * 16 + 8 * j + 2 * t));
-            const uint32_t scB = e4m3x2_to_f16x2(lds_u16(stage + GT_CODES + (rl + 8) * 16 + 8 * j + 2 * t));
-            sa[mt][0] = dup_lo(scA); sa[mt][1] = dup_hi(scA);
-            sb[mt][0] = dup_lo(scB); sb[mt][1] = dup_hi(scB);
-          }
-          const uint32_t xs = stage + GT_CODES + GT_SCALES + j * NT * 2048 + lane * 16;
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint32_t A0[MT][4], A1[MT][4];
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              uint32_t fa[4], fb[4];
-              e2m1x8_to_f16x2(wa[mt][w], fa);
-              e2m1x8_to_f16x2(wb[mt][w], fb);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                fa[e] = hmul2(fa[e], sa[mt][w >> 1]);
-                fb[e] = hmul2(fb[e], sb[mt][w >> 1]);
-              }
-              A0[mt][0] = fa[0]; A0[mt][1] = fb[0]; A0[mt][2] = fa[1]; A0[mt][3] = fb[1];
-              A1[mt][0] = fa[2]; A1[mt][1] = fb[2]; A1[mt][2] = fa[3]; A1[mt][3] = fb[3];
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              const uint4 bx = lds_v4(xs + (nt * 4 + w) * 512);
-#pragma unroll
-              for (int mt = 0; mt < MT; ++mt) {
-                mma_f16_16816(acc[mt][nt], A0[mt], bx.x, bx.y);
-                mma_f16_16816(acc[mt][nt], A1[mt], bx.z, bx.w);
-              }
-            }
-          }
+          gt_mma_iteration<NT, MT>(stage, j, grp, sw, t, lane, acc);
         }
       }
       __syncwarp();

@@ -4,13 +4,16 @@
 //   route:    top-k of softmax(router logits), ties to the lower expert id
 //   plan:     group the T*k routed rows by expert, each expert padded to a
 //             multiple of 32 rows (one token chunk of the skinny kernel)
-//   gate/up:  [g; u] = x @ W13_e^T, h = bf16(silu(g) * u)      (skinny kernel)
-//   down:     y = h @ W2_e^T, fp32                              (skinny kernel)
+//   gate/up:  [g; u] = x @ W13_e^T, h = bf16(silu(g) * u)
+//   down:     y = h @ W2_e^T, fp32
+// (both on the TMA-fed skinny kernel when K is a multiple of 256, else on the
+// register-fed one)
 //   combine:  out[t] = bf16(sum_j w[t][j] * y[pos(t, j)]), slots in order
 // The order in which routed rows land inside an expert's group comes from
 // atomics, but every row's arithmetic is independent of its position, so the
 // output is deterministic.
 #include "gemv_core.cuh"
+#include "gemv_tma.cuh"
 #include "launch.h"
 
 namespace nvfp4 {
@@ -117,19 +120,27 @@ __global__ void count_kernel(const int32_t* ids, int64_t R, int E, int* counts) 
 }
 
 // Single CTA: padded offsets, the chunk table, and row_of = -1 everywhere.
+// The counts are staged in shared memory first, so the (serial, in-order)
+// prefix sum runs on shared-memory latency.
+constexpr int PLAN_MAX_E = 4096;
 __global__ void plan_kernel(const int* counts, int E, int* poff, int* chunk_count, int* chunk_expert,
                             int* chunk_rows, int* row_of) {
   __shared__ int s_total;
+  __shared__ int s_pad[PLAN_MAX_E];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_pad[e] = (counts[e] + GV_MCHUNK - 1) / GV_MCHUNK * GV_MCHUNK;
+  __syncthreads();
   if (threadIdx.x == 0) {
     int acc = 0;
     for (int e = 0; e < E; ++e) {
-      poff[e] = acc;
-      acc += (counts[e] + GV_MCHUNK - 1) / GV_MCHUNK * GV_MCHUNK;
+      const int n = s_pad[e];
+      s_pad[e] = acc;
+      acc += n;
     }
     s_total = acc;
     *chunk_count = acc / GV_MCHUNK;
   }
   __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) poff[e] = s_pad[e];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int n = counts[e];
     const int c0 = poff[e] / GV_MCHUNK;
@@ -155,10 +166,10 @@ __global__ void scatter_kernel(const int32_t* ids, int64_t R, int topk, int E, c
   pos_of[i] = pos;
 }
 
-// One CTA per padded row: gather (tokens) or pass through (h), to fragments.
-__global__ void __launch_bounds__(GV_THREADS) xprep_moe_kernel(const uint16_t* src, int64_t K, bool gather,
-                                                                const int* row_of, const int* chunk_count,
-                                                                uint4* xfrag, int* pexp) {
+// One CTA per padded row (rows longer than MOE_PREP_MAX_K).
+__global__ void __launch_bounds__(GV_THREADS) xprep_moe_row_kernel(const uint16_t* src, int64_t K, bool gather,
+                                                                    const int* row_of, const int* chunk_count,
+                                                                    uint4* xfrag, int* pexp) {
   const int64_t r = blockIdx.x;
   if (r >= static_cast<int64_t>(*chunk_count) * GV_MCHUNK) return;
   const int tok = row_of[r];
@@ -167,17 +178,122 @@ __global__ void __launch_bounds__(GV_THREADS) xprep_moe_kernel(const uint16_t* s
   xprep_row(s, K, r, xfrag, pexp);
 }
 
+// One warp per padded row: gather (tokens) or pass through (h), to
+// fragments. The warp reads its row once into registers (K <= 4096), takes
+// the amax with shuffles and converts (the same per-row shift and rounding as
+// xprep_row).
+constexpr int MOE_PREP_WARPS = 8;
+constexpr int MOE_PREP_MAX_K = 4096;
+__global__ void __launch_bounds__(MOE_PREP_WARPS * 32) xprep_moe_kernel(const uint16_t* src, int64_t K, bool gather,
+                                                                         const int* row_of, const int* chunk_count,
+                                                                         uint4* xfrag, int* pexp) {
+  constexpr int CH = MOE_PREP_MAX_K / 8 / 32;   // 16-byte chunks per lane
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * MOE_PREP_WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= static_cast<int64_t>(*chunk_count) * GV_MCHUNK) return;
+  const int tok = row_of[r];
+  const uint16_t* s = nullptr;
+  if (tok >= 0) s = gather ? src + static_cast<int64_t>(tok) * K : src + r * K;
+  const int64_t n8 = K / 8;
+  uint4 v[CH];
+  float amax = 0.f;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int64_t q = lane + 32 * c;
+    v[c] = make_uint4(0, 0, 0, 0);
+    if (s != nullptr && q < n8) v[c] = __ldg(reinterpret_cast<const uint4*>(s) + q);
+    const uint32_t w4[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] & 0xFFFFu)));
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] >> 16)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  int p = 0;
+  if (amax > 0.f) p = min(max(ilogbf(amax) - 14, -100), 113);
+  const float mul = ldexpf(1.0f, -p);
+  if (lane == 0) pexp[r] = p;
+  const int64_t chunk = r / GV_MCHUNK;
+  const int nt = static_cast<int>((r % GV_MCHUNK) / 8);
+  const int g = static_cast<int>(r % 8);
+  const int64_t n_it = K / GV_KIT;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int64_t q = lane + 32 * c;
+    if (q < n8) {
+      uint4 o;
+      o.x = f32x2_to_f16x2(bf16_bits_to_f32(v[c].x & 0xFFFFu) * mul, bf16_bits_to_f32(v[c].x >> 16) * mul);
+      o.y = f32x2_to_f16x2(bf16_bits_to_f32(v[c].y & 0xFFFFu) * mul, bf16_bits_to_f32(v[c].y >> 16) * mul);
+      o.z = f32x2_to_f16x2(bf16_bits_to_f32(v[c].z & 0xFFFFu) * mul, bf16_bits_to_f32(v[c].z >> 16) * mul);
+      o.w = f32x2_to_f16x2(bf16_bits_to_f32(v[c].w & 0xFFFFu) * mul, bf16_bits_to_f32(v[c].w >> 16) * mul);
+      const int64_t it = q / 16;
+      const int rem = static_cast<int>(q % 16);
+      xfrag[xfrag_unit(chunk, n_it, it, nt, rem % 4, g * 4 + rem / 4)] = o;
+    }
+  }
+}
+
+// out[t][c] = bf16(sum_j w[t][j] * y[pos(t, j)][c]), slots in order; one
+// thread per 4 columns (H % 4 == 0), CTA (t, column block of 1024).
 __global__ void combine_kernel(const float* ybuf, const int* pos_of, const float* w, int64_t T, int topk,
                                int64_t H, uint16_t* out) {
   const int64_t t = blockIdx.x;
-  for (int64_t c = threadIdx.x; c < H; c += blockDim.x) {
-    float acc = 0.f;
-    for (int j = 0; j < topk; ++j) {
-      const int pos = pos_of[t * topk + j];
-      if (pos >= 0) acc = fmaf(w[t * topk + j], ybuf[static_cast<int64_t>(pos) * H + c], acc);
-    }
-    out[t * H + c] = static_cast<uint16_t>(f32_to_bf16_bits(acc));
+  const int64_t c = (static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x) * 4;
+  if (c >= H) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < topk; ++j) {
+    const int pos = pos_of[t * topk + j];
+    if (pos < 0) continue;
+    const float wj = w[t * topk + j];
+    const float4 y = *reinterpret_cast<const float4*>(ybuf + static_cast<int64_t>(pos) * H + c);
+    acc.x = fmaf(wj, y.x, acc.x);
+    acc.y = fmaf(wj, y.y, acc.y);
+    acc.z = fmaf(wj, y.z, acc.z);
+    acc.w = fmaf(wj, y.w, acc.w);
   }
+  uint2 o;
+  o.x = f32_to_bf16_bits(acc.x) | (f32_to_bf16_bits(acc.y) << 16);
+  o.y = f32_to_bf16_bits(acc.z) | (f32_to_bf16_bits(acc.w) << 16);
+  *reinterpret_cast<uint2*>(out + t * H + c) = o;
+}
+
+// One expert GEMM on the TMA-fed skinny kernel: one CTA per (32-token chunk,
+// row tile), CTAs of unused chunks exit at once. W is the stack of the E
+// experts' matrices, viewed as one [E * rows][K] matrix; box_rows = 64 for
+// gate/up (64 gate rows and the matching 64 up rows per tile), 128 for down.
+template <int MODE>
+int launch_moe_tma(const nvfp4_tensor_t& W, int box_rows, const TmaSkinnyParams& p, dim3 grid, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(W.batch) * W.rows;
+  CUtensorMap mc, ms;
+  int rc = make_tmap_2d_u8(&mc, W.codes, W.K / 2, rows, W.K / 2, 128, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != NVFP4_OK) return rc;
+  rc = make_tmap_2d_u8(&ms, W.scales, W.K / 16, rows, W.K / 16, 16, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != NVFP4_OK) return rc;
+  auto k = skinny_tma_kernel<4, MODE, 2, 2>;
+  rc = ensure_smem(k, GtCfg<4>::SMEM);
+  if (rc != NVFP4_OK) return rc;
+  return launch_ex(k, grid, dim3(GtWarps<2, 2>::THREADS), GtCfg<4>::SMEM, 1, false, stream, mc, ms, p);
+}
+
+// Activation prep of the routed rows (K = H: gather tokens; K = I: pass h through).
+int prep_moe(const uint16_t* src, int64_t K, bool gather, const MoeWs& m, uint4* xfrag, int* pexp,
+             cudaStream_t stream) {
+  const int64_t prow = m.max_chunks * GV_MCHUNK;
+  if (K <= MOE_PREP_MAX_K)
+    xprep_moe_kernel<<<static_cast<unsigned>(ceil_div(prow, MOE_PREP_WARPS)), MOE_PREP_WARPS * 32, 0, stream>>>(
+        src, K, gather, m.row_of, m.chunk_count, xfrag, pexp);
+  else
+    xprep_moe_row_kernel<<<static_cast<unsigned>(prow), GV_THREADS, 0, stream>>>(src, K, gather, m.row_of,
+                                                                                  m.chunk_count, xfrag, pexp);
+  return from_cuda(cudaGetLastError());
+}
+
+int combine(const MoeWs& m, const float* w, int64_t T, int topk, int64_t H, uint16_t* out, cudaStream_t stream) {
+  combine_kernel<<<dim3(static_cast<unsigned>(T), static_cast<unsigned>(ceil_div(H, 1024))), 256, 0, stream>>>(
+      m.ybuf, m.pos_of, w, T, topk, H, out);
+  return from_cuda(cudaGetLastError());
 }
 
 }  // namespace
@@ -201,6 +317,7 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
   if (T == 0) return NVFP4_OK;
   const int64_t E = W13.batch, I = W13.rows / 2, H = W13.K;
   const int64_t R = T * topk;
+  if (E > PLAN_MAX_E) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   const MoeWs m = carve_moe(ws, T, H, I, E, topk);
   if (cudaMemsetAsync(m.counts, 0, m.zero_bytes, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
   const unsigned gr = static_cast<unsigned>(ceil_div(R, 256));
@@ -209,10 +326,43 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
                                       m.chunk_rows, m.row_of);
   scatter_kernel<<<gr, 256, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.cursor, m.row_of,
                                          m.pos_of);
-  const unsigned prow = static_cast<unsigned>(m.max_chunks * GV_MCHUNK);
-  xprep_moe_kernel<<<prow, GV_THREADS, 0, stream>>>(X, H, true, m.row_of, m.chunk_count, m.xfrag1, m.pexp1);
-  int rc = from_cuda(cudaGetLastError());
+  int rc = prep_moe(X, H, true, m, m.xfrag1, m.pexp1, stream);
   if (rc != NVFP4_OK) return rc;
+
+  if (H % 256 == 0 && I % 256 == 0) {
+    TmaSkinnyParams p{};
+    p.s_t = W13.s_t;
+    p.K = H;
+    p.xfrag = m.xfrag1;
+    p.pexp = m.pexp1;
+    p.split = 1;
+    p.chunk_count = m.chunk_count;
+    p.chunk_expert = m.chunk_expert;
+    p.chunk_rows = m.chunk_rows;
+    p.inter = I;
+    p.hidden = H;
+    p.rows_per_expert = 2 * I;
+    p.h_out = m.hbuf;
+    p.status = device_status_ptr();
+    rc = launch_moe_tma<SK_MOE_GATEUP>(W13, 64, p,
+                                       dim3(static_cast<unsigned>(m.max_chunks), static_cast<unsigned>(I / 64)),
+                                       stream);
+    if (rc != NVFP4_OK) return rc;
+    rc = prep_moe(m.hbuf, I, false, m, m.xfrag2, m.pexp2, stream);
+    if (rc != NVFP4_OK) return rc;
+    TmaSkinnyParams q = p;
+    q.s_t = W2.s_t;
+    q.K = I;
+    q.xfrag = m.xfrag2;
+    q.pexp = m.pexp2;
+    q.rows_per_expert = H;
+    q.h_out = nullptr;
+    q.y_out = m.ybuf;
+    rc = launch_moe_tma<SK_MOE_DOWN>(
+        W2, 128, q, dim3(static_cast<unsigned>(m.max_chunks), static_cast<unsigned>(ceil_div(H, GV_ROWS))), stream);
+    if (rc != NVFP4_OK) return rc;
+    return combine(m, w, T, topk, H, out, stream);
+  }
 
   SkinnyParams p{};
   p.codes = W13.codes;
@@ -234,9 +384,7 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
                       0, 1, stream, p);
   if (rc != NVFP4_OK) return rc;
 
-  xprep_moe_kernel<<<prow, GV_THREADS, 0, stream>>>(m.hbuf, I, false, m.row_of, m.chunk_count, m.xfrag2,
-                                                    m.pexp2);
-  rc = from_cuda(cudaGetLastError());
+  rc = prep_moe(m.hbuf, I, false, m, m.xfrag2, m.pexp2, stream);
   if (rc != NVFP4_OK) return rc;
 
   SkinnyParams q = p;
@@ -254,8 +402,7 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
                       dim3(GV_THREADS), 0, 1, stream, q);
   if (rc != NVFP4_OK) return rc;
 
-  combine_kernel<<<static_cast<unsigned>(T), 256, 0, stream>>>(m.ybuf, m.pos_of, w, T, topk, H, out);
-  return from_cuda(cudaGetLastError());
+  return combine(m, w, T, topk, H, out, stream);
 }
 
 }  // namespace nvfp4
