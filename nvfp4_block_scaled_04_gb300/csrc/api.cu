@@ -24,25 +24,29 @@ int sm_count() {
 }
 
 int ensure_smem_impl(const void* func, int bytes) {
+  // per (kernel, device): the largest dynamic shared-memory size set so far
+  // (a kernel whose size depends on the shape may need more on a later call)
+  constexpr int kMaxFuncs = 256, kMaxDevs = 64;
   static std::mutex mu;
-  static const void* funcs[256];
-  static unsigned long long devmask[256];
+  static const void* funcs[kMaxFuncs];
+  static int set_bytes[kMaxFuncs][kMaxDevs];
   static int n = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
-  const unsigned long long bit = 1ull << (dev & 63);
+  if (dev < 0 || dev >= kMaxDevs) return NVFP4_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(mu);
   int i = 0;
   while (i < n && funcs[i] != func) ++i;
-  if (i < n && (devmask[i] & bit)) return NVFP4_OK;
+  if (i < n && set_bytes[i][dev] >= bytes) return NVFP4_OK;
   if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
     return NVFP4_ERR_CUDA;
   if (i == n) {
-    if (n == 256) return NVFP4_OK;
+    if (n == kMaxFuncs) return NVFP4_OK;
     funcs[n] = func;
-    devmask[n++] = 0;
+    for (int d = 0; d < kMaxDevs; ++d) set_bytes[n][d] = 0;
+    ++n;
   }
-  devmask[i] |= bit;
+  set_bytes[i][dev] = bytes;
   return NVFP4_OK;
 }
 

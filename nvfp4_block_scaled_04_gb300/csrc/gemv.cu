@@ -72,6 +72,21 @@ int launch_tma_plain_nt(const TmaSkinnyParams& p, const CUtensorMap& mc, const C
   return launch_ex(k, grid, dim3(GtWarps<MT, KW>::THREADS), GtCfg<NT>::SMEM, 1, true, stream, mc, ms, p);
 }
 
+// GEMV with argmax on the TMA-fed kernel (split 1). With an index the codes
+// and scales come in by tile::gather4 of one-row-high boxes (GATHER), over
+// the whole weight by 2-D boxes of 128 rows.
+template <int NT, bool GATHER>
+int launch_tma_argmax_nt(const TmaSkinnyParams& p, const CUtensorMap& mc, const CUtensorMap& ms, dim3 grid,
+                         cudaStream_t stream) {
+  constexpr int MT = NT >= 2 ? 2 : 1;
+  constexpr int KW = NT >= 2 ? 2 : 1;
+  using C = GtCfg<NT, GATHER ? GT_SCALES_GATHERED : GT_SCALES>;
+  auto k = skinny_tma_kernel<NT, SK_ARGMAX, MT, KW, GATHER>;
+  int rc = ensure_smem(k, C::SMEM);
+  if (rc != NVFP4_OK) return rc;
+  return launch_ex(k, grid, dim3(GtWarps<MT, KW>::THREADS), C::SMEM, 1, true, stream, mc, ms, p);
+}
+
 // Split-K of the TMA-fed GEMV: as many K-slices per 128-row tile as still fit
 // in one wave of two CTAs per SM (at most 8, at least one stage each).
 int tma_split(int64_t tiles, int64_t n_stages) { return choose_split(tiles, n_stages); }
@@ -196,6 +211,69 @@ int launch_gather_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, 
   if (rc != NVFP4_OK) return rc;
   const int64_t n_it = K / GV_KIT;
   const int64_t row_tiles = ceil_div(n_idx, GV_ROWS);
+  const RsLayout rs = rs_layout(K);
+  if (idx && nt == 1 && K % 256 == 0 && rs.smem <= 227 * 1024) {
+    // masked rows, one n-tile: stream whole candidate rows
+    TmaSkinnyParams q{};
+    q.s_t = W.s_t;
+    q.K = K;
+    q.n_rows = n_idx;
+    q.xfrag = w.xfrag;
+    q.pexp = w.pexp;
+    q.M = M;
+    q.split = 1;
+    q.status = device_status_ptr();
+    q.idx = idx;
+    q.keys = w.keys;
+    q.counter = w.counter;
+    q.out_ids = out_ids;
+    q.out_logit = out_logit;
+    q.codes = W.codes;
+    q.scales = W.scales;
+    rc = ensure_smem(gather_rows_argmax_kernel, rs.smem);
+    if (rc != NVFP4_OK) return rc;
+    const int64_t groups = ceil_div(n_idx, RS_ROWS);
+    const int64_t grid = groups < sm_count() ? groups : sm_count();
+    return launch_ex(gather_rows_argmax_kernel, dim3(static_cast<unsigned>(grid)), dim3(RS_THREADS), rs.smem, 1, true,
+                     stream, q, rs);
+  }
+  if (K % 256 == 0) {
+    CUtensorMap mc, ms;
+    const int box_rows = idx ? 1 : GV_ROWS;
+    rc = make_tmap_2d_u8(&mc, W.codes, K / 2, W.rows, K / 2, 128, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != NVFP4_OK) return rc;
+    rc = make_tmap_2d_u8(&ms, W.scales, K / 16, W.rows, K / 16, 16, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc != NVFP4_OK) return rc;
+    TmaSkinnyParams q{};
+    q.s_t = W.s_t;
+    q.K = K;
+    q.n_rows = n_idx;
+    q.xfrag = w.xfrag;
+    q.pexp = w.pexp;
+    q.M = M;
+    q.split = 1;
+    q.status = device_status_ptr();
+    q.idx = idx;
+    q.keys = w.keys;
+    q.counter = w.counter;
+    q.out_ids = out_ids;
+    q.out_logit = out_logit;
+    const dim3 grid(1, static_cast<unsigned>(row_tiles), 1);
+    if (idx) {
+      switch (nt) {
+        case 1: return launch_tma_argmax_nt<1, true>(q, mc, ms, grid, stream);
+        case 2: return launch_tma_argmax_nt<2, true>(q, mc, ms, grid, stream);
+        case 3: return launch_tma_argmax_nt<3, true>(q, mc, ms, grid, stream);
+        default: return launch_tma_argmax_nt<4, true>(q, mc, ms, grid, stream);
+      }
+    }
+    switch (nt) {
+      case 1: return launch_tma_argmax_nt<1, false>(q, mc, ms, grid, stream);
+      case 2: return launch_tma_argmax_nt<2, false>(q, mc, ms, grid, stream);
+      case 3: return launch_tma_argmax_nt<3, false>(q, mc, ms, grid, stream);
+      default: return launch_tma_argmax_nt<4, false>(q, mc, ms, grid, stream);
+    }
+  }
   SkinnyParams p{};
   p.codes = W.codes;
   p.scales = W.scales;

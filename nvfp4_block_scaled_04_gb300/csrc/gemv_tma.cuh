@@ -37,10 +37,21 @@ struct GtWarps {
 constexpr int GT_CODES = 128 * 128;      // one stage of codes: 128 rows x 128 bytes
 constexpr int GT_SCALES = 128 * 16;      // one stage of scales: 128 rows x 16 bytes
 
-template <int NT>
+// Scales of gathered rows: tile::gather4 writes a lane's four 16-byte rows
+// to one 128-byte-aligned slot (a tensor copy's shared-memory destination
+// must be 128-byte aligned), so row r sits at (r / 4) * 128 + (r % 4) * 16.
+constexpr int GT_SCALES_GATHERED = 128 * 32;
+
+template <bool GATHERED>
+NVFP4_DEV uint32_t gt_scale_row(int r) {
+  return GATHERED ? static_cast<uint32_t>((r >> 2) * 128 + (r & 3) * 16) : static_cast<uint32_t>(r * 16);
+}
+
+template <int NT, int SC = GT_SCALES>
 struct GtCfg {
+  static constexpr int SCALES = SC;                                           // scale area of a stage
   static constexpr int XB = 2 * NT * 2048;                                    // activations of 2 iterations
-  static constexpr int STAGE = (GT_CODES + GT_SCALES + XB + 1023) / 1024 * 1024;
+  static constexpr int STAGE = (GT_CODES + SC + XB + 1023) / 1024 * 1024;
   static constexpr int STAGES = NT <= 2 ? 4 : 3;
   static constexpr int RING = STAGES * STAGE;
   static constexpr int SMEM = RING + 1024 /*alignment*/ + 512 /*barriers, shifts, flags*/;
@@ -66,6 +77,14 @@ struct TmaSkinnyParams {
   int* status;
   float* partials;             // split-K > 1: [tile][split][32 tokens][128 rows] fp32
   unsigned int* counters;      // split-K > 1: one arrival counter per tile, zeroed by the prep kernel
+  // ARGMAX (split 1): candidate j is weight row idx[j] (row j when idx is null)
+  const int32_t* idx;
+  unsigned long long* keys;    // [M] best (logit order key, ~id) so far, zero on entry
+  unsigned int* counter;       // finished CTAs, zero on entry
+  int32_t* out_ids;
+  float* out_logit;            // nullable
+  const uint8_t* codes;        // row-streaming ARGMAX: the weight itself
+  const uint8_t* scales;
 };
 
 // MMA row g of a warp's 16-row tile reads shared-memory row sigma(g) (and
@@ -90,8 +109,9 @@ NVFP4_DEV uint4 lds_v4(uint32_t saddr) {
 // (row group grp) against NT n-tiles of 8 tokens; j selects the iteration
 // within the stage (codes at 16-byte chunks 4j..4j+3 of each 128-byte row,
 // scales at bytes 8j..8j+7, activation fragments at j * NT * 2048).
-template <int NT, int MT>
+template <int NT, int MT, bool GATHERED = false>
 NVFP4_DEV void gt_mma_iteration(uint32_t stage, int j, int grp, int sw, int t, int lane, float (&acc)[MT][NT][4]) {
+  constexpr int SC = GATHERED ? GT_SCALES_GATHERED : GT_SCALES;
   const uint32_t phys = static_cast<uint32_t>(((4 * j + t) ^ sw) << 4);
   uint32_t wa[MT][4], wb[MT][4], sa[MT][2], sb[MT][2];
 #pragma unroll
@@ -101,12 +121,12 @@ NVFP4_DEV void gt_mma_iteration(uint32_t stage, int j, int grp, int sw, int t, i
     const uint4 cb = lds_v4(stage + (rl + 8) * 128 + phys);
     wa[mt][0] = ca.x; wa[mt][1] = ca.y; wa[mt][2] = ca.z; wa[mt][3] = ca.w;
     wb[mt][0] = cb.x; wb[mt][1] = cb.y; wb[mt][2] = cb.z; wb[mt][3] = cb.w;
-    const uint32_t scA = e4m3x2_to_f16x2(lds_u16(stage + GT_CODES + rl * 16 + 8 * j + 2 * t));
-    const uint32_t scB = e4m3x2_to_f16x2(lds_u16(stage + GT_CODES + (rl + 8) * 16 + 8 * j + 2 * t));
+    const uint32_t scA = e4m3x2_to_f16x2(lds_u16(stage + GT_CODES + gt_scale_row<GATHERED>(rl) + 8 * j + 2 * t));
+    const uint32_t scB = e4m3x2_to_f16x2(lds_u16(stage + GT_CODES + gt_scale_row<GATHERED>(rl + 8) + 8 * j + 2 * t));
     sa[mt][0] = dup_lo(scA); sa[mt][1] = dup_hi(scA);
     sb[mt][0] = dup_lo(scB); sb[mt][1] = dup_hi(scB);
   }
-  const uint32_t xs = stage + GT_CODES + GT_SCALES + j * NT * 2048 + lane * 16;
+  const uint32_t xs = stage + GT_CODES + SC + j * NT * 2048 + lane * 16;
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
     uint32_t A0[MT][4], A1[MT][4];
@@ -135,11 +155,14 @@ NVFP4_DEV void gt_mma_iteration(uint32_t stage, int j, int grp, int sw, int t, i
   }
 }
 
-template <int NT, int MODE, int MT, int KW>
+// GATHER (ARGMAX with an index only): weight rows come in by tile::gather4;
+// otherwise by 2-D boxes of consecutive rows.
+template <int NT, int MODE, int MT, int KW, bool GATHER = false>
 __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
     skinny_tma_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
                       const TmaSkinnyParams p) {
-  using C = GtCfg<NT>;
+  constexpr bool GATHERED = MODE == SK_ARGMAX && GATHER;
+  using C = GtCfg<NT, GATHERED ? GT_SCALES_GATHERED : GT_SCALES>;
   pdl_launch_dependents();   // the next call's activation prep may queue up now
   constexpr int NCW = GtWarps<MT, KW>::CONSUMERS;
   constexpr int NGR = GtWarps<MT, KW>::GROUPS;
@@ -152,6 +175,8 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
   int* pexp_s = reinterpret_cast<int*>(ring_ptr + C::RING + 64);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ring_ptr + C::RING + 64 + 128);
   int* s_last = reinterpret_cast<int*>(ring_ptr + C::RING + 64 + 132);
+  unsigned long long* kbest = reinterpret_cast<unsigned long long*>(ring_ptr + C::RING + 256);   // ARGMAX, [32]
+  static_assert(2 * C::STAGES * 8 <= 64, "barrier area");
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
 
@@ -193,6 +218,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_codes) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_scales) : "memory");
   }
+  if (MODE == SK_ARGMAX && tid < GV_MCHUNK) kbest[tid] = 0ull;
   __syncthreads();
 
   float acc[MT][NT][4];
@@ -204,7 +230,64 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
       for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
 
   int issued = 0;
-  if (warp == NCW) {
+  if (GATHERED && warp == NCW) {
+    // Gathered rows: lane l loads candidate rows 4l .. 4l+3 of the tile with
+    // one tile::gather4 per stage for the codes (4 x 128 bytes, 128B swizzle,
+    // so they land exactly where a 2-D box would put them) and one for the
+    // scales (4 x 16 bytes). Candidates past the end repeat the last row;
+    // the epilogue ignores them.
+    int rid[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t j0 = row_tile * GV_ROWS + 4 * lane + i;
+      const int64_t j = j0 < p.n_rows ? j0 : p.n_rows - 1;
+      rid[i] = p.idx ? p.idx[j] : static_cast<int>(j);
+    }
+    auto issue_weights = [&](int st) {
+      const int q = st % C::STAGES;
+      const uint32_t stage = ring + q * C::STAGE;
+      // bytes that land: 32 lanes x (4 x 128 code bytes + 4 x 16 scale bytes)
+      if (lane == 0)
+        mbar_arrive_expect_tx(full_bar(q), GT_CODES + GT_SCALES + 2 * NT * 2048 + (st == 0 ? 128u : 0u));
+      __syncwarp();
+      const int xc = static_cast<int>((it0 + 2LL * st) * 64);
+      const int xs = static_cast<int>((it0 + 2LL * st) * 8);
+      tma_gather4(stage + lane * 512, &map_codes, xc, rid[0], rid[1], rid[2], rid[3], full_bar(q));
+      tma_gather4(stage + GT_CODES + lane * 128, &map_scales, xs, rid[0], rid[1], rid[2], rid[3], full_bar(q));
+    };
+    auto issue_x = [&](int st) {
+      const int q = st % C::STAGES;
+      const uint32_t stage = ring + q * C::STAGE;
+      if (st == 0) bulk_load(smem_addr(pexp_s), p.pexp + chunk * GV_MCHUNK, 128u, full_bar(q));
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        bulk_load(stage + GT_CODES + C::SCALES + j * NT * 2048,
+                  p.xfrag + xfrag_unit(chunk, n_it, it0 + 2LL * st + j, 0, 0, 0), NT * 2048u, full_bar(q));
+    };
+    // Stages go out in pairs: a lane requests K-chunks st and st + 1 of its
+    // four rows back to back, 256 contiguous bytes per row, so the random
+    // rows cost one DRAM page opening per 256 bytes instead of per 128.
+    const int pre = n_st < C::STAGES ? n_st : C::STAGES;
+    for (int st = 0; st < pre; ++st) issue_weights(st);
+    pdl_wait();   // the activation prep has finished and its writes are visible
+    if (lane == 0)
+      for (int st = 0; st < pre; ++st) issue_x(st);
+    issued = pre;
+    for (int st = pre; st < n_st; st += 2) {
+      const int n = st + 1 < n_st ? 2 : 1;
+      bool ok = true;
+      for (int u = 0; u < n && ok; ++u) {
+        const int q = (st + u) % C::STAGES;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_bounded(empty_bar(q), (((st + u) / C::STAGES) - 1) & 1, abort_flag, p.status));
+      }
+      if (!ok) break;
+      for (int u = 0; u < n; ++u) issue_weights(st + u);
+      if (lane == 0)
+        for (int u = 0; u < n; ++u) issue_x(st + u);
+      issued += n;
+    }
+  } else if (warp == NCW) {
     if (lane == 0) {
       // y coordinates of the tile's rows in the stacked weight
       int y_a, y_b = 0;
@@ -272,7 +355,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
       for (int jj = 0; jj < 3 - KW; ++jj) {
         const int j = KW == 2 ? jk : jj;
         if (it0 + 2LL * st + j < it_end) {
-          gt_mma_iteration<NT, MT>(stage, j, grp, sw, t, lane, acc);
+          gt_mma_iteration<NT, MT, GATHERED>(stage, j, grp, sw, t, lane, acc);
         }
       }
       __syncwarp();
@@ -318,6 +401,14 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
       if (MODE == SK_PLAIN) {
         const int64_t n = row_tile * GV_ROWS + r;
         if (n < p.n_rows) p.Y[(row_base + tok) * p.n_rows + n] = static_cast<uint16_t>(f32_to_bf16_bits(v * mul));
+      } else if (MODE == SK_ARGMAX) {
+        // key: logit order first, then the lower vocabulary id
+        const int64_t j = row_tile * GV_ROWS + r;
+        if (j < p.n_rows) {
+          const uint32_t vid = p.idx ? static_cast<uint32_t>(p.idx[j]) : static_cast<uint32_t>(j);
+          atomicMax(&kbest[tok],
+                    (static_cast<unsigned long long>(float_order_key(v * mul)) << 32) | (0xFFFFFFFFu - vid));
+        }
       } else if (MODE == SK_MOE_GATEUP) {
         const float gg = v * mul;
         const float uu = psum(tok, 64 + r) * mul;
@@ -326,6 +417,25 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
       } else {
         const int64_t c = row_tile * GV_ROWS + r;
         if (c < p.hidden) p.y_out[(row_base + tok) * p.hidden + c] = v * mul;
+      }
+    }
+    if (MODE == SK_ARGMAX) {
+      // this CTA's per-token best into the global keys; the last CTA to
+      // finish reads them out and leaves keys and counter at zero
+      __syncthreads();
+      if (tid < rows_in_chunk) atomicMax(&p.keys[row_base + tid], kbest[tid]);
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) *s_last = atomicAdd(p.counter, 1u) == gridDim.x * gridDim.y * gridDim.z - 1;
+      __syncthreads();
+      if (*s_last) {
+        __threadfence();
+        for (int64_t m = tid; m < p.M; m += NTHR) {
+          const unsigned long long key = atomicExch(&p.keys[m], 0ull);
+          p.out_ids[m] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+          if (p.out_logit) p.out_logit[m] = float_from_order_key(static_cast<uint32_t>(key >> 32));
+        }
+        if (tid == 0) atomicExch(p.counter, 0u);
       }
     }
   } else if (MODE == SK_PLAIN) {
@@ -357,6 +467,199 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
               static_cast<uint16_t>(f32_to_bf16_bits(v * ldexpf(st, pexp_s[tok])));
       }
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Gathered-row GEMV with argmax, row-streaming form (one 8-token n-tile).
+// Candidate rows are random rows of the weight, so they are fetched whole:
+// per stage, 16 candidates x full K, each row's codes and scales with one
+// bulk copy each (a few large copies instead of many 128-byte tile gathers).
+// The activation fragments of the whole K sit in shared memory for the
+// kernel's lifetime. One persistent CTA per SM walks row groups b, b + G, ...
+//   warps 0..7  consumers: warp w takes K-iterations [w n_it / 8, (w+1) n_it / 8)
+//               of the stage's 16 rows; partial logits meet in a
+//               double-buffered area, one named barrier per stage
+//   warp 8      producer (lanes 0..15 copy one row's codes and scales each)
+constexpr int RS_ROWS = 16;
+constexpr int RS_STAGES = 2;
+constexpr int RS_CONSUMERS = 8;
+constexpr int RS_PRODUCER = RS_CONSUMERS;
+constexpr int RS_THREADS = (RS_CONSUMERS + 1) * 32;
+
+struct RsLayout {
+  int code_stride, scale_stride, stage_bytes, x_bytes, smem;
+};
+// Row strides padded so that the 8 rows an MMA phase reads fall in distinct
+// banks (code rows 64 bytes apart modulo 128).
+inline RsLayout rs_layout(int64_t K) {
+  RsLayout l;
+  l.code_stride = static_cast<int>(K / 2 + 64);
+  l.scale_stride = static_cast<int>(K / 16 + 16);
+  l.stage_bytes = (RS_ROWS * (l.code_stride + l.scale_stride) + 127) / 128 * 128;
+  l.x_bytes = static_cast<int>(K / GV_KIT) * 2048;
+  l.smem = l.x_bytes + RS_STAGES * l.stage_bytes + 2 * RS_CONSUMERS * RS_ROWS * 8 * 4 + 1024 + 512;
+  return l;
+}
+
+static __global__ void __launch_bounds__(RS_THREADS, 1)
+    gather_rows_argmax_kernel(const TmaSkinnyParams p, RsLayout L) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t xs = base;
+  const uint32_t ring = base + L.x_bytes;
+  float* red = reinterpret_cast<float*>(base_ptr + L.x_bytes + RS_STAGES * L.stage_bytes);
+  uint8_t* tail = base_ptr + L.x_bytes + RS_STAGES * L.stage_bytes + 2 * RS_CONSUMERS * RS_ROWS * 8 * 4;
+  const uint32_t bar_base = smem_addr(tail);
+  auto full_bar = [&](int q) { return bar_base + 8u * q; };
+  auto empty_bar = [&](int q) { return bar_base + 8u * (RS_STAGES + q); };
+  const uint32_t x_bar = bar_base + 8u * (2 * RS_STAGES);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tail + 64);
+  int* s_last = reinterpret_cast<int*>(tail + 68);
+  unsigned long long* kbest = reinterpret_cast<unsigned long long*>(tail + 128);   // [8]
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int64_t KB = p.K / 2, KS = p.K / 16;
+  const int n_it = static_cast<int>(p.K / GV_KIT);
+  const int64_t n_groups = (p.n_rows + RS_ROWS - 1) / RS_ROWS;
+  const int n_mine = static_cast<int>((n_groups - blockIdx.x + gridDim.x - 1) / gridDim.x);
+
+  if (tid == 0) {
+    for (int q = 0; q < RS_STAGES; ++q) {
+      mbar_init(full_bar(q), 1);
+      mbar_init(empty_bar(q), RS_CONSUMERS);
+    }
+    mbar_init(x_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid < 8) kbest[tid] = 0ull;
+  __syncthreads();
+
+  if (warp == RS_PRODUCER) {
+    // producer: lane r < 16 copies candidate row r of the group
+    auto issue = [&](int i) {
+      const int q = i % RS_STAGES;
+      const uint32_t stage = ring + q * L.stage_bytes;
+      const int64_t group = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+      if (lane == 0) mbar_arrive_expect_tx(full_bar(q), static_cast<uint32_t>(RS_ROWS * (KB + KS)));
+      __syncwarp();
+      if (lane < RS_ROWS) {
+        const int64_t j0 = group * RS_ROWS + lane;
+        const int64_t j = j0 < p.n_rows ? j0 : p.n_rows - 1;
+        const int64_t v = p.idx ? static_cast<int64_t>(p.idx[j]) : j;
+        bulk_load(stage + lane * L.code_stride, p.codes + v * KB, static_cast<uint32_t>(KB), full_bar(q));
+        bulk_load(stage + RS_ROWS * L.code_stride + lane * L.scale_stride, p.scales + v * KS,
+                  static_cast<uint32_t>(KS), full_bar(q));
+      }
+    };
+    const int pre = n_mine < RS_STAGES ? n_mine : RS_STAGES;
+    for (int i = 0; i < pre; ++i) issue(i);
+    pdl_wait();   // the activation prep has finished and its writes are visible
+    if (lane == 0) {
+      mbar_arrive_expect_tx(x_bar, static_cast<uint32_t>(n_it) * 2048u);
+      for (int it = 0; it < n_it; ++it)
+        bulk_load(xs + it * 2048, p.xfrag + xfrag_unit(0, n_it, it, 0, 0, 0), 2048u, x_bar);
+    }
+    int issued = pre;
+    for (int i = pre; i < n_mine; ++i) {
+      const int q = i % RS_STAGES;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(empty_bar(q), ((i / RS_STAGES) - 1) & 1, abort_flag, p.status)))
+        break;
+      issue(i);
+      ++issued;
+    }
+    // after a give-up, let the copies in flight land before the CTA exits
+    if (lane == 0 && *abort_flag) {
+      mbar_wait_bounded(x_bar, 0, nullptr, p.status, 100000000ull);
+      const int first = issued > RS_STAGES ? issued - RS_STAGES : 0;
+      for (int i = first; i < issued; ++i)
+        mbar_wait_bounded(full_bar(i % RS_STAGES), (i / RS_STAGES) & 1, nullptr, p.status, 100000000ull);
+    }
+  } else {
+    pdl_wait();   // the per-token shifts come from the prep
+    const int it0 = warp * n_it / RS_CONSUMERS, it1 = (warp + 1) * n_it / RS_CONSUMERS;
+    const float st = p.s_t[0];
+    const int M = static_cast<int>(p.M);
+    bool x_ready = false;
+    for (int i = 0; i < n_mine; ++i) {
+      const int q = i % RS_STAGES;
+      float acc[1][1][4] = {{{0.f, 0.f, 0.f, 0.f}}};
+      const bool ok = !*abort_flag && (x_ready || (x_ready = mbar_wait_bounded(x_bar, 0, abort_flag, p.status))) &&
+                      mbar_wait_bounded(full_bar(q), (i / RS_STAGES) & 1, abort_flag, p.status);
+      if (ok) {
+        const uint32_t stage = ring + q * L.stage_bytes;
+        const uint32_t rowA = stage + g * L.code_stride + t * 16;
+        const uint32_t rowB = rowA + 8 * L.code_stride;
+        const uint32_t scA0 = stage + RS_ROWS * L.code_stride + g * L.scale_stride + 2 * t;
+        const uint32_t scB0 = scA0 + 8 * L.scale_stride;
+        for (int it = it0; it < it1; ++it) {
+          const uint4 ca = lds_v4(rowA + it * 64);
+          const uint4 cb = lds_v4(rowB + it * 64);
+          const uint32_t scA = e4m3x2_to_f16x2(lds_u16(scA0 + it * 8));
+          const uint32_t scB = e4m3x2_to_f16x2(lds_u16(scB0 + it * 8));
+          const uint32_t sa[2] = {dup_lo(scA), dup_hi(scA)}, sb[2] = {dup_lo(scB), dup_hi(scB)};
+          const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w}, wb[4] = {cb.x, cb.y, cb.z, cb.w};
+          const uint32_t xb = xs + it * 2048 + lane * 16;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint32_t fa[4], fb[4];
+            e2m1x8_to_f16x2(wa[w], fa);
+            e2m1x8_to_f16x2(wb[w], fb);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              fa[e] = hmul2(fa[e], sa[w >> 1]);
+              fb[e] = hmul2(fb[e], sb[w >> 1]);
+            }
+            const uint32_t A0[4] = {fa[0], fb[0], fa[1], fb[1]}, A1[4] = {fa[2], fb[2], fa[3], fb[3]};
+            const uint4 bx = lds_v4(xb + w * 512);
+            mma_f16_16816(acc[0][0], A0, bx.x, bx.y);
+            mma_f16_16816(acc[0][0], A1, bx.z, bx.w);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(q));
+      }
+      // partial logits of this warp: rows g, g + 8, tokens 2t, 2t + 1
+      float* rb = red + (i & 1) * (RS_CONSUMERS * RS_ROWS * 8) + warp * (RS_ROWS * 8);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) rb[(g + 8 * (e >> 1)) * 8 + 2 * t + (e & 1)] = acc[0][0][e];
+      asm volatile("bar.sync 1, %0;" ::"r"(RS_CONSUMERS * 32) : "memory");
+      if (tid < RS_ROWS * 8) {
+        const int r = tid >> 3, tok = tid & 7;
+        const int64_t j = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) * RS_ROWS + r;
+        if (tok < M && j < p.n_rows) {
+          const float* rr = red + (i & 1) * (RS_CONSUMERS * RS_ROWS * 8) + r * 8 + tok;
+          float v = 0.f;
+#pragma unroll
+          for (int w = 0; w < RS_CONSUMERS; ++w) v += rr[w * RS_ROWS * 8];
+          const uint32_t vid = p.idx ? static_cast<uint32_t>(p.idx[j]) : static_cast<uint32_t>(j);
+          atomicMax(&kbest[tok], (static_cast<unsigned long long>(float_order_key(v * ldexpf(st, p.pexp[tok])))
+                                  << 32) | (0xFFFFFFFFu - vid));
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // this CTA's per-token best into the global keys; the last CTA to finish
+  // reads them out and leaves keys and counter at zero
+  const int rows_in_chunk = static_cast<int>(p.M);
+  if (tid < rows_in_chunk) atomicMax(&p.keys[tid], kbest[tid]);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) *s_last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (*s_last) {
+    __threadfence();
+    for (int64_t m = tid; m < p.M; m += RS_THREADS) {
+      const unsigned long long key = atomicExch(&p.keys[m], 0ull);
+      p.out_ids[m] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+      if (p.out_logit) p.out_logit[m] = float_from_order_key(static_cast<uint32_t>(key >> 32));
+    }
+    if (tid == 0) atomicExch(p.counter, 0u);
   }
 }
 
