@@ -441,30 +441,54 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
   } else if (MODE == SK_PLAIN) {
     // split-K: partials to global memory, the last CTA of the tile reduces
     const int64_t tile = chunk * gridDim.y + row_tile;
-    float* mine = p.partials + ((tile * S + s) * GV_MCHUNK) * GV_ROWS;
-    for (int e = tid; e < rows_in_chunk * GV_ROWS; e += NTHR) mine[e] = psum(e / GV_ROWS, e % GV_ROWS);
+    constexpr int P4 = GV_MCHUNK * GV_ROWS / 4;   // float4 groups of one split's partial
+    float4* mine = reinterpret_cast<float4*>(p.partials) + (tile * S + s) * P4;
+    const int n4 = rows_in_chunk * (GV_ROWS / 4);  // groups in use: [token][128 rows / 4]
+    for (int e4 = tid; e4 < n4; e4 += NTHR) {
+      const int tok = e4 >> 5, r = (e4 & 31) * 4;
+      mine[e4] = make_float4(psum(tok, r), psum(tok, r + 1), psum(tok, r + 2), psum(tok, r + 3));
+    }
     __threadfence();
     __syncthreads();
     if (tid == 0) *s_last = atomicAdd(&p.counters[tile], 1u) == static_cast<unsigned>(S - 1);
     __syncthreads();
     if (*s_last) {
       __threadfence();
-      const float* all = p.partials + (tile * S * GV_MCHUNK) * GV_ROWS;
-      for (int e = tid; e < rows_in_chunk * GV_ROWS; e += NTHR) {
-        const int tok = e / GV_ROWS;
-        const int r = e % GV_ROWS;
-        // all S (<= 8) partials in flight at once, summed in split order
-        float x[8];
+      const float4* all = reinterpret_cast<const float4*>(p.partials) + tile * S * P4;
+      // two groups per thread per round, all S (<= 8) partials of both requested before any
+      // is summed: the reduction costs one or two L2 round trips, not one per output
+      for (int b = tid; b < n4; b += 2 * NTHR) {
+        float4 x[2][8];
 #pragma unroll
-        for (int qq = 0; qq < 8; ++qq) x[qq] = qq < S ? __ldcg(all + (qq * GV_MCHUNK + tok) * GV_ROWS + r) : 0.f;
-        float v = 0.f;
+        for (int u = 0; u < 2; ++u) {
+          const int e4 = b + u * NTHR;
 #pragma unroll
-        for (int qq = 0; qq < 8; ++qq)
-          if (qq < S) v += x[qq];
-        const int64_t n = row_tile * GV_ROWS + r;
-        if (n < p.n_rows)
-          p.Y[(row_base + tok) * p.n_rows + n] =
-              static_cast<uint16_t>(f32_to_bf16_bits(v * ldexpf(st, pexp_s[tok])));
+          for (int qq = 0; qq < 8; ++qq)
+            x[u][qq] = (qq < S && e4 < n4) ? __ldcg(all + qq * P4 + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int e4 = b + u * NTHR;
+          if (e4 >= n4) continue;
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int qq = 0; qq < 8; ++qq)   // split order: deterministic
+            if (qq < S) v = make_float4(v.x + x[u][qq].x, v.y + x[u][qq].y, v.z + x[u][qq].z, v.w + x[u][qq].w);
+          const int tok = e4 >> 5;
+          const int64_t n = row_tile * GV_ROWS + (e4 & 31) * 4;
+          const float mul = ldexpf(st, pexp_s[tok]);
+          uint16_t* dst = p.Y + (row_base + tok) * p.n_rows + n;
+          const uint32_t lo = f32x2_to_bf16x2(v.x * mul, v.y * mul), hi = f32x2_to_bf16x2(v.z * mul, v.w * mul);
+          if (n + 3 < p.n_rows && (p.n_rows & 3) == 0) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+          } else {
+            const uint16_t o4[4] = {static_cast<uint16_t>(lo), static_cast<uint16_t>(lo >> 16),
+                                    static_cast<uint16_t>(hi), static_cast<uint16_t>(hi >> 16)};
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              if (n + c < p.n_rows) dst[c] = o4[c];
+          }
+        }
       }
     }
   }

@@ -28,7 +28,7 @@ def test_tiny_config():
 
 
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 9, 17, 32, 33, 70])
-@pytest.mark.parametrize("N,K", [(512, 256), (200, 384), (136, 1280)])
+@pytest.mark.parametrize("N,K", [(512, 256), (200, 384), (136, 1280), (200, 512)])
 def test_shapes(M, N, K):
     w = synth.normal_f32((N, K), 0.02, seed=N + K)
     x = synth.normal_bf16((M, K), seed=M)
@@ -97,3 +97,28 @@ def test_split_k_is_deterministic_and_matches_unsplit_shape():
     assert torch.equal(a, b)
     ref = O.gemm_w4a16(x.float().numpy(), O.quantize(w.numpy()))
     assert O.rel_fro(np_f64(a), ref) <= TOL
+
+
+@pytest.mark.parametrize("N,K", [(256, 2048), (128, 8192)])
+def test_activation_magnitude_changes_along_k(N, K):
+    """Tokens whose magnitude jumps between 256-element stretches of K: the
+    in-kernel conversion raises its power-of-two shift mid-row and rescales
+    the accumulators (the second shape also splits K across CTAs)."""
+    w = synth.normal_f32((N, K), 0.02, seed=71)
+    x = synth.normal_f32((7, K), 1.0, seed=72)
+    nb = K // 256
+    b = torch.arange(nb, dtype=torch.float32)
+    blocks = torch.stack([
+        2.0 ** (4 * b),                                  # growing
+        2.0 ** (-4 * b),                                 # shrinking
+        torch.where(b < nb // 2, 0.0, 1.0),              # zeros, then values
+        torch.where(b == nb - 1, 3e30, 1.0),             # one huge stretch at the end
+        torch.zeros(nb),                                 # all zero
+        torch.where(b % 2 == 0, 1e-20, 1e20),            # alternating tiny / huge
+        torch.ones(nb),
+    ])
+    x = (x * blocks.repeat_interleave(256, dim=1)).to(torch.bfloat16)
+    y, ref = run(w, x)
+    assert np.all(y[4] == 0.0)
+    for r in (0, 1, 2, 3, 5, 6):
+        assert O.rel_fro(y[r], ref[r]) <= TOL, r
