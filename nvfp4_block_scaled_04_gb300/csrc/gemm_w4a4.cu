@@ -377,6 +377,328 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair version (cta_group::2), used once M spans two 128-row tiles.
+//
+// Each SM receives TMA data at about 55 bytes per clock whatever the other
+// SMs do (measured on GB300 with L2-resident tiles), so with one CTA per
+// 128 x 256 tile the 54 KB a stage brings in takes longer than the four MMAs
+// it feeds. Two CTAs of a cluster share one 256 x 256 tile: each holds its
+// own 128 rows of A and one 128-row half of the W tile, and one thread of the
+// even CTA issues tcgen05.mma.cta_group::2 (M = 256), which reads both CTAs'
+// shared memory and accumulates each CTA's 128 rows into that CTA's tensor
+// memory. Per stage an SM now takes in 38 KB (A 16, W half 16, the A scales
+// 2 and the whole W tile's scales 4) for the same MMA work.
+//
+// Synchronisation, per CTA unless stated:
+//   full[s]   TMA bytes of this CTA's stage s landed (its producers)
+//   ready[s]  in the even CTA only: both CTAs' scale warps have put stage s's
+//             scales into their tensor memory (8 arrivals, 4 remote)
+//   empty[s]  the pair's MMAs have consumed stage s (one multicast commit)
+//   accf      the tile's accumulation is complete (one multicast commit)
+//   acce      in the even CTA only: both CTAs' epilogues have drained the
+//             accumulator (16 arrivals, 8 remote)
+// Every wait is bounded; both CTAs reach the closing cluster barrier on every
+// path, so a CTA never leaves while its peer may still touch its memory.
+constexpr int P_STAGES = 5;
+constexpr int P_B_BYTES = 128 * 128;                                   // one 128-row half of the W tile
+constexpr int P_STAGE_BYTES = A_BYTES + P_B_BYTES + SFA_BYTES + SFB_BYTES;   // 38 KB
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + 1024 + 256;
+static_assert(SF_TMEM_BASE + P_STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "tensor memory columns");
+static_assert((3 * P_STAGES + 4) * 8 <= 256, "barrier area");
+constexpr int P_BAND = 16;                                             // m-pairs that share one sweep over W
+// kind::mxf4nvf4, E2M1 x E2M1, K-major, N = 256, M = 256 (the pair)
+constexpr uint32_t P_IDESC = (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(256 >> 4) << 24);
+
+NVFP4_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on a barrier that threads of the peer CTA arrive on.
+NVFP4_DEV bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 0;; ++n) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((n & 63) == 63) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+        atomicExch(&g_device_status, NVFP4_ERR_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Arrive on the barrier at the same shared-memory offset in CTA `rank` of the cluster.
+NVFP4_DEV void mbar_arrive_cluster(uint32_t bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(rank));
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+NVFP4_DEV void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa, uint32_t sfb,
+                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %6, [%3], [%4], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(sfa), "r"(sfb), "r"(accumulate), "r"(P_IDESC)
+      : "memory");
+}
+
+// Arrive once on the barrier at this offset in both CTAs of the pair when the
+// MMAs issued so far have completed.
+NVFP4_DEV void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+// pair tile -> (m_pair, n_tile): bands of P_BAND m-pairs sweep all n-tiles
+NVFP4_DEV void pair_coords(int tile, int m_pairs, int n_tiles, int& m_pair, int& n_tile) {
+  const int band = tile / (P_BAND * n_tiles);
+  const int band_m0 = band * P_BAND;
+  const int band_h = min(P_BAND, m_pairs - band_m0);
+  const int within = tile - band * P_BAND * n_tiles;
+  m_pair = band_m0 + within % band_h;
+  n_tile = within / band_h;
+}
+
+// Warp roles as in gemm_w4a4_kernel, in both CTAs; in the odd CTA warp 1 only
+// takes part in the tensor-memory allocation.
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                          const W4A4Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bar_base = base + P_STAGES * P_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + P_STAGES * P_STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * P_STAGES + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * P_STAGES + 3);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (P_STAGES + s); };
+  auto ready_bar = [&](int s) { return bar_base + 8u * (2 * P_STAGES + s); };
+  const uint32_t accf_bar = bar_base + 8u * (3 * P_STAGES);
+  const uint32_t acce_bar = bar_base + 8u * (3 * P_STAGES + 1);
+  auto stage_a = [&](int s) { return base + s * P_STAGE_BYTES; };
+  auto stage_b = [&](int s) { return base + s * P_STAGE_BYTES + A_BYTES; };
+  auto stage_sfa = [&](int s) { return base + s * P_STAGE_BYTES + A_BYTES + P_B_BYTES; };
+  auto stage_sfb = [&](int s) { return base + s * P_STAGE_BYTES + A_BYTES + P_B_BYTES + SFA_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair_id = static_cast<int>(blockIdx.x >> 1), n_pairs = static_cast<int>(gridDim.x >> 1);
+  const int m_pairs = (p.m_tiles + 1) / 2;
+  const int n_tiles_total = m_pairs * p.n_tiles;
+  const int n_k = (p.K + BK - 1) / BK;
+  const int k_atoms_total = p.K / 64;
+  const int64_t sf_row_stride = static_cast<int64_t>(k_atoms_total) * 512;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(ready_bar(s), 2 * SF_WARPS);
+    }
+    mbar_init(accf_bar, 1);
+    mbar_init(acce_bar, 2 * EPI_WARPS);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_a) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_b) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();   // both CTAs' barriers and tensor memory exist before anything refers to them
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  int next_it = 0;
+  int mma_tiles = 0;
+  const int prod = warp == 0 ? 0 : (warp == 2 ? 1 : -1);
+
+  if (prod >= 0) {
+    if (lane == 0) {
+      int it = 0;
+      for (int tile = pair_id; tile < n_tiles_total && !*abort_flag; tile += n_pairs) {
+        int m_pair, n_tile;
+        pair_coords(tile, m_pairs, p.n_tiles, m_pair, n_tile);
+        const int m_tile = 2 * m_pair + static_cast<int>(rank);
+        // an odd CTA past the last m-tile reads the last real scale strip; its rows are never stored
+        const int rt_a = min(m_tile, p.m_tiles - 1);
+        const int rt_b0 = 2 * n_tile;
+        const int rt_b1 = min(2 * n_tile + 1, (p.N + 127) / 128 - 1);
+        bool ok = true;
+        for (int ks = 0; ks < n_k; ++ks, ++it) {
+          if ((it & 1) != prod) continue;
+          const int s = it % P_STAGES;
+          if (it >= P_STAGES && !mbar_wait_cluster(empty_bar(s), ((it / P_STAGES) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int atoms = min(4, k_atoms_total - 4 * ks);
+          const uint32_t sf_bytes = static_cast<uint32_t>(atoms) * 512u;
+          mbar_arrive_expect_tx(full_bar(s), A_BYTES + P_B_BYTES + 3u * sf_bytes);
+          tma_load_2d(stage_a(s), &map_a, ks * 128, m_tile * BM, full_bar(s));
+          tma_load_2d(stage_b(s), &map_b, ks * 128, n_tile * BN + static_cast<int>(rank) * 128, full_bar(s));
+          bulk_load(stage_sfa(s), p.sfa + rt_a * sf_row_stride + static_cast<int64_t>(ks) * 2048, sf_bytes,
+                    full_bar(s));
+          bulk_load(stage_sfb(s), p.sfb + rt_b0 * sf_row_stride + static_cast<int64_t>(ks) * 2048, sf_bytes,
+                    full_bar(s));
+          bulk_load(stage_sfb(s) + 2048, p.sfb + rt_b1 * sf_row_stride + static_cast<int64_t>(ks) * 2048, sf_bytes,
+                    full_bar(s));
+          next_it = it + 1;
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (rank == 0 && lane == 0) {
+      int it = 0;
+      for (int tile = pair_id; tile < n_tiles_total && !*abort_flag; tile += n_pairs) {
+        // both CTAs' epilogues must have drained the previous tile's accumulator
+        if (mma_tiles > 0 && !mbar_wait_cluster(acce_bar, (mma_tiles - 1) & 1, abort_flag)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int ks = 0; ks < n_k; ++ks, ++it) {
+          const int s = it % P_STAGES;
+          // both CTAs' scale warps arrive only after their stage's copies landed
+          if (!mbar_wait_cluster(ready_bar(s), (it / P_STAGES) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int atoms = min(4, k_atoms_total - 4 * ks);
+          const uint32_t sf_col = tmem + SF_TMEM_BASE + s * SF_COLS_PER_STAGE;
+          for (int k = 0; k < atoms; ++k) {
+            const uint64_t adesc = smem_desc(stage_a(s) + 32 * k, 16, 1024, 2);
+            const uint64_t bdesc = smem_desc(stage_b(s) + 32 * k, 16, 1024, 2);
+            tc_mma_pair(tmem, adesc, bdesc, sf_col + 4 * k, sf_col + 16 + 8 * k, (ks > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit_pair(empty_bar(s));
+        }
+        if (!ok) break;
+        tc_commit_pair(accf_bar);
+        ++mma_tiles;
+      }
+    }
+  } else if (warp < SF_WARP0) {
+    const int quarter = warp & 3;
+    const int half = (warp - EPI_WARP0) >> 2;
+    const float scale = p.st_a[0] * p.st_b[0];
+    int done = 0;
+    for (int tile = pair_id; tile < n_tiles_total; tile += n_pairs, ++done) {
+      int m_pair, n_tile;
+      pair_coords(tile, m_pairs, p.n_tiles, m_pair, n_tile);
+      if (!__all_sync(0xffffffffu, mbar_wait_cluster(accf_bar, done & 1, abort_flag))) break;
+      tc_fence_after();
+      uint32_t packed[64];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc_ld_32cols(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(half * 128 + 32 * c), r);
+        tc_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          packed[16 * c + q] = f32x2_to_bf16x2(__uint_as_float(r[2 * q]) * scale, __uint_as_float(r[2 * q + 1]) * scale);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acce_bar, 0);
+      const int row = (2 * m_pair + static_cast<int>(rank)) * BM + quarter * 32 + lane;
+      const int col0 = n_tile * BN + half * 128;
+      if (row < p.M && col0 < p.N) {
+        uint16_t* dst = p.Y + static_cast<int64_t>(row) * p.N + col0;
+        const int nq = (p.N - col0) >= 128 ? 16 : (p.N - col0) / 8;
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          if (q < nq)
+            reinterpret_cast<uint4*>(dst)[q] =
+                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+      }
+    }
+  } else {
+    // scale warps: this CTA's A scales and the whole W tile's scales into its
+    // own tensor memory (layout as in gemm_w4a4_kernel), then tell the even CTA
+    const uint32_t lane_cols = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + SF_TMEM_BASE;
+    int it = 0;
+    for (int tile = pair_id; tile < n_tiles_total; tile += n_pairs) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      bool ok = true;
+      for (int ks = 0; ks < n_k; ++ks, ++it) {
+        const int s = it % P_STAGES;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_bounded(full_bar(s), (it / P_STAGES) & 1, abort_flag, &g_device_status))) {
+          ok = false;
+          break;
+        }
+        uint32_t v[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 x = lds128(stage_sfa(s) + 512 * k + 16 * lane);
+          v[4 * k] = x.x, v[4 * k + 1] = x.y, v[4 * k + 2] = x.z, v[4 * k + 3] = x.w;
+        }
+        const uint32_t col = lane_cols + s * SF_COLS_PER_STAGE;
+        tc_st_16cols(col, v);
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint4 x = lds128(stage_sfb(s) + 2048 * h + 512 * (2 * pr + kk) + 16 * lane);
+              const int o = 8 * kk + 4 * h;
+              v[o] = x.x, v[o + 1] = x.y, v[o + 2] = x.z, v[o + 3] = x.w;
+            }
+          tc_st_16cols(col + 16 + 16 * pr, v);
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(ready_bar(s), 0);
+      }
+      if (!ok) break;
+    }
+  }
+
+  // Unwind: copies and MMAs already issued land (bounded) before the memory they target goes away.
+  if (prod >= 0 && lane == 0 && *abort_flag) {
+    for (int it = next_it - 1; it >= 0 && it >= next_it - 2 * P_STAGES; --it)
+      if ((it & 1) == prod)
+        mbar_wait_bounded(full_bar(it % P_STAGES), (it / P_STAGES) & 1, nullptr, &g_device_status, 100000000ull);
+  }
+  if (warp == 1 && rank == 0 && lane == 0 && *abort_flag && mma_tiles > 0) {
+    mbar_wait_bounded(accf_bar, (mma_tiles - 1) & 1, nullptr, &g_device_status, 100000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // the peer is done with this CTA's shared and tensor memory
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
 // One CTA waits on an mbarrier that nothing arrives on: the bounded wait must
 // give up, record NVFP4_ERR_TIMEOUT and free the tensor memory it took.
 __global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns) {
@@ -456,6 +778,18 @@ int launch_gemm_w4a4(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t*
   p.K = static_cast<int>(K);
   p.m_tiles = static_cast<int>(ceil_div(M, BM));
   p.n_tiles = static_cast<int>(ceil_div(N, BN));
+  if (p.m_tiles >= 2) {
+    // CTA pairs on 256 x 256 tiles: W tiles come in 128-row halves
+    rc = make_code_map(&map_b, W.codes, N, K, 128);
+    if (rc != NVFP4_OK) return rc;
+    rc = ensure_smem(gemm_w4a4_pair_kernel, P_SMEM_BYTES);
+    if (rc != NVFP4_OK) return rc;
+    const int64_t pair_tiles = ceil_div(p.m_tiles, 2) * p.n_tiles;
+    const int64_t max_pairs = sm_count() / 2;
+    const unsigned grid = static_cast<unsigned>(2 * (pair_tiles < max_pairs ? pair_tiles : max_pairs));
+    return launch_ex(gemm_w4a4_pair_kernel, dim3(grid), dim3(THREADS), P_SMEM_BYTES, 2, false, stream, map_a, map_b,
+                     p);
+  }
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
   const unsigned grid = static_cast<unsigned>(tiles < sm_count() ? tiles : sm_count());
   gemm_w4a4_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(map_a, map_b, p);

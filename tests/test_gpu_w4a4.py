@@ -22,7 +22,7 @@ def gpu_gemm(a_bf16, w_f32, a_layout=1, w_layout=1):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 256, 512), (200, 136, 320), (1, 8, 64),
-                                   (384, 512, 1024), (130, 264, 576)])
+                                   (384, 512, 1024), (130, 264, 576), (640, 256, 256), (1024, 520, 768)])
 @pytest.mark.parametrize("layouts", [(1, 1), (0, 0)])
 def test_shapes(M, N, K, layouts):
     a = synth.student_t_bf16((M, K), 4, seed=M)
@@ -32,12 +32,15 @@ def test_shapes(M, N, K, layouts):
     assert O.rel_fro(y, ref) <= TOL, (M, N, K, O.rel_fro(y, ref))
 
 
-def test_exact_special_case_is_bit_exact():
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 256, 512), (384, 264, 320), (640, 520, 1024),
+                                   (4096, 4096, 128)])
+def test_exact_special_case_is_bit_exact(M, N, K):
     """Unit scales and s_t = 1 on both sides: products of e2m1 codes are exact
-    and every partial sum is a small multiple of 1/4, so the output is exact."""
+    and every partial sum is a small multiple of 1/4, so the output is exact.
+    M > 128 runs the CTA-pair kernel (odd m-tile counts, ragged N and K; the
+    largest shape gives each CTA pair several tiles in turn)."""
     m = nv()
     rng = np.random.default_rng(2)
-    M, N, K = 128, 128, 256
     ca = rng.integers(0, 16, (M, K)).astype(np.uint8)
     cw = rng.integers(0, 16, (N, K)).astype(np.uint8)
     one = np.full((M, K // 16), 0x38, np.uint8)
