@@ -62,6 +62,9 @@ int ensure_smem(Kernel kernel, int bytes) {
 // ---- tma_host.cu: 2-D uint8 tensor map (inner dimension contiguous).
 int make_tmap_2d_u8(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t row_stride,
                     int box_inner, int box_outer, int swizzle);
+// 2-D 16-bit map (e.g. a bf16 output), rows of row_stride_bytes.
+int make_tmap_2d_u16(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t row_stride_bytes,
+                     int box_inner, int box_outer, int swizzle);
 
 // ---- gemm_w4a4.cu: device address of the status word bounded waits write.
 int* device_status_ptr();
