@@ -204,6 +204,35 @@ int nvfp4_gather_gemv_argmax(const void* H, int64_t M, nvfp4_tensor_t W,
                              float* out_logit, void* workspace, size_t workspace_bytes,
                              nvfp4_stream_t stream);
 
+/* Compact copy of selected rows of an NVFP4 matrix: row j of the output is
+ * row idx[j] of W (its packed codes and its row-major block scales; the
+ * tensor scale is W's and stays with the caller). A one-time prepack for a
+ * fixed row subset such as the draft head's mask ("The masked head trick",
+ * Serving Qwen3.8-27B...), so that every draft step then streams the subset as
+ * one dense matrix.
+ *   W           NVFP4 [V][K], batch 1, ROWMAJOR scales; K a multiple of 32
+ *   idx         device int32 [n_idx]; an entry outside [0, V) yields a zero row
+ *               and sets NVFP4_ERR_INVALID_ARG in the device status word
+ *               (nvfp4_read_device_status)
+ *   codes_out   device, n_idx * K/2 bytes, 16-byte aligned
+ *   scales_out  device, n_idx * K/16 bytes */
+int nvfp4_gather_rows(nvfp4_tensor_t W, const int32_t* idx, int64_t n_idx, uint8_t* codes_out,
+                      uint8_t* scales_out, nvfp4_stream_t stream);
+
+/* GEMV with a fused argmax over every row of W, reporting ids through a map:
+ *   logit[m][j]  = sum_k H[m][k] * W_hat[j][k]   (fp32 accumulation)
+ *   out_ids[m]   = ids[argmax_j logit[m][j]] (j when ids == NULL); among equal
+ *                  logits the lowest reported id wins
+ *   out_logit[m] = that maximum logit, if out_logit != NULL.
+ * With W the nvfp4_gather_rows copy of a head's masked rows and ids the mask,
+ * this is the masked draft head of nvfp4_gather_gemv_argmax on a compact
+ * matrix (same result, same bytes streamed per step).
+ *   H   device bf16 [M][K], 1 <= M <= 32;  W NVFP4, batch 1, ROWMAJOR,
+ *       K a multiple of 256;  ids device int32 [W.rows] or NULL
+ *   workspace >= nvfp4_workspace_size(NVFP4_OP_GATHER_ARGMAX, M, W.rows, K, 0, 0). */
+int nvfp4_gemv_argmax(const void* H, int64_t M, nvfp4_tensor_t W, const int32_t* ids, int32_t* out_ids,
+                      float* out_logit, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
 /* ---- helpers --------------------------------------------------------------- */
 
 /* Bytes of one matrix's block scales in the given layout. */

@@ -16,6 +16,7 @@ import torch
 LIB_PATH = Path(__file__).resolve().parent / "libnvfp4.so"
 
 OK = 0
+ERR_INVALID_ARG, ERR_TIMEOUT = -1, -6
 DTYPE_F32, DTYPE_BF16 = 0, 1
 ST_COMPUTE, ST_GIVEN = 0, 1
 SCALES_ROWMAJOR, SCALES_MMA = 0, 1
@@ -23,7 +24,7 @@ OP_QUANTIZE, OP_GEMM_W4A16, OP_GEMM_W4A4, OP_GROUPED_GEMM, OP_GATHER_ARGMAX = ra
 
 EXPORTS = [
     "nvfp4_quantize", "nvfp4_prepack_scales", "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4",
-    "nvfp4_moe_route", "nvfp4_grouped_gemm", "nvfp4_gather_gemv_argmax",
+    "nvfp4_moe_route", "nvfp4_grouped_gemm", "nvfp4_gather_gemv_argmax", "nvfp4_gather_rows", "nvfp4_gemv_argmax",
     "nvfp4_scales_bytes", "nvfp4_workspace_size", "nvfp4_status_string",
     "nvfp4_read_device_status", "nvfp4_selftest_bounded_wait", "nvfp4_version",
     "nvfp4_gemm_w4a16_noalloc",
@@ -57,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_moe_route.argtypes = [vp, i64, i32, i32, vp, vp, vp]
         L.nvfp4_grouped_gemm.argtypes = [vp, i64, i32, vp, vp, CTensor, CTensor, vp, vp, sz, vp]
         L.nvfp4_gather_gemv_argmax.argtypes = [vp, i64, CTensor, vp, i64, vp, vp, vp, sz, vp]
+        L.nvfp4_gather_rows.argtypes = [CTensor, vp, i64, vp, vp, vp]
+        L.nvfp4_gemv_argmax.argtypes = [vp, i64, CTensor, vp, vp, vp, vp, sz, vp]
         L.nvfp4_scales_bytes.argtypes = [i64, i64, i32]
         L.nvfp4_scales_bytes.restype = sz
         L.nvfp4_workspace_size.argtypes = [i32, i64, i64, i64, i64, i64]
@@ -227,6 +230,30 @@ def gather_gemv_argmax(h: torch.Tensor, w: QTensor, idx: torch.Tensor | None = N
     _check(lib().nvfp4_gather_gemv_argmax(_ptr(h), M, w.c(), _ptr(idx), n_idx, _ptr(ids), _ptr(logit),
                                           _ptr(ws), ws.numel(), _stream()), "nvfp4_gather_gemv_argmax")
     return ids, logit
+
+
+def gather_rows(w: QTensor, idx: torch.Tensor) -> QTensor:
+    """Compact NVFP4 copy of rows idx of w (one-time prepack of a fixed row subset)."""
+    _require_cuda(w.codes, idx)
+    n = idx.numel()
+    codes = torch.empty(n, w.K // 2, dtype=torch.uint8, device=w.codes.device)
+    scales = torch.empty(max(n * (w.K // 16), 1), dtype=torch.uint8, device=w.codes.device)
+    _check(lib().nvfp4_gather_rows(w.c(), _ptr(idx), n, _ptr(codes), _ptr(scales), _stream()), "nvfp4_gather_rows")
+    return QTensor(codes, scales, w.s_t, n, w.K)
+
+
+def gemv_argmax(h: torch.Tensor, w: QTensor, ids: torch.Tensor | None = None,
+                workspace: torch.Tensor | None = None):
+    """Argmax over all rows of w, row j reported as ids[j]: (ids int32 [M], max logit fp32 [M])."""
+    _require_cuda(h)
+    M = h.shape[0]
+    out = torch.empty(M, dtype=torch.int32, device=h.device)
+    logit = torch.empty(M, dtype=torch.float32, device=h.device)
+    ws = workspace if workspace is not None else _workspace(
+        workspace_size(OP_GATHER_ARGMAX, M, w.rows, w.K), h.device)
+    _check(lib().nvfp4_gemv_argmax(_ptr(h), M, w.c(), _ptr(ids), _ptr(out), _ptr(logit), _ptr(ws), ws.numel(),
+                                   _stream()), "nvfp4_gemv_argmax")
+    return out, logit
 
 
 def read_device_status() -> int:

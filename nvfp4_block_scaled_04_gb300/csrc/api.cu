@@ -188,6 +188,27 @@ int nvfp4_gather_gemv_argmax(const void* H, int64_t M, nvfp4_tensor_t W, const i
                               reinterpret_cast<cudaStream_t>(stream));
 }
 
+int nvfp4_gather_rows(nvfp4_tensor_t W, const int32_t* idx, int64_t n_idx, uint8_t* codes_out,
+                      uint8_t* scales_out, nvfp4_stream_t stream) {
+  if (!idx || !codes_out || !scales_out || n_idx < 0 || !tensor_ok(W) || W.batch != 1) return NVFP4_ERR_INVALID_ARG;
+  if (W.scale_layout != NVFP4_SCALES_ROWMAJOR) return NVFP4_ERR_INVALID_ARG;
+  if (W.K % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;   // whole 16-byte pieces of codes per row
+  if (!aligned16(W.codes) || !aligned16(codes_out)) return NVFP4_ERR_MISALIGNED;
+  if (n_idx == 0) return NVFP4_OK;
+  return launch_gather_rows(W, idx, n_idx, codes_out, scales_out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int nvfp4_gemv_argmax(const void* H, int64_t M, nvfp4_tensor_t W, const int32_t* ids, int32_t* out_ids,
+                      float* out_logit, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+  if (!H || !out_ids || M < 1 || M > 32 || !tensor_ok(W) || W.batch != 1 || W.rows < 1) return NVFP4_ERR_INVALID_ARG;
+  if (W.scale_layout != NVFP4_SCALES_ROWMAJOR) return NVFP4_ERR_INVALID_ARG;
+  if (W.K % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(H) || !aligned16(W.codes) || !aligned16(W.scales)) return NVFP4_ERR_MISALIGNED;
+  if (!workspace || workspace_bytes < argmax_workspace_bytes(M, W.K)) return NVFP4_ERR_WORKSPACE;
+  return launch_gemv_argmax(static_cast<const uint16_t*>(H), M, W, ids, out_ids, out_logit, workspace,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
 int nvfp4_read_device_status(int* out, nvfp4_stream_t stream) {
   if (!out) return NVFP4_ERR_INVALID_ARG;
   return read_device_status(out, reinterpret_cast<cudaStream_t>(stream));

@@ -11,7 +11,8 @@ namespace {
 
 // One CTA per output row of a dense activation matrix X[M][K] (rows beyond
 // M, up to the n-tile padding of the chunk, become zeros).
-// CTA (0, 0) also zeroes the split-K arrival counters of the GEMV that follows.
+// CTA (0, 0) also zeroes the split-K arrival counters (or the argmax keys and
+// completion counter) of the kernel that follows.
 // 1024 threads per row: up to K = 32768 the row is read once, into registers.
 // Launched as a programmatic dependent of whatever kernel precedes it on the
 // stream: it lets its own GEMV launch at once (that GEMV starts streaming its
@@ -32,6 +33,25 @@ __global__ void __launch_bounds__(XPREP_THREADS) xprep_dense_kernel(const uint16
   else if (n8 <= 2 * XPREP_THREADS) xprep_row_regs<2>(src, K, out_row, xfrag, pexp);
   else if (n8 <= 4 * XPREP_THREADS) xprep_row_regs<4>(src, K, out_row, xfrag, pexp);
   else xprep_row(src, K, out_row, xfrag, pexp);
+}
+
+// Row j of the compact copy = row idx[j] of W (codes and row-major scales),
+// one warp per row, 16-byte copies. An index outside [0, rows) gives a zero
+// row and NVFP4_ERR_INVALID_ARG in the device status word.
+__global__ void gather_rows_kernel(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t K,
+                                   const int32_t* idx, int64_t n_idx, uint8_t* codes_out, uint8_t* scales_out,
+                                   int* status) {
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (j >= n_idx) return;
+  const int64_t v = idx[j];
+  const bool ok = v >= 0 && v < rows;
+  if (!ok && lane == 0) atomicExch(status, NVFP4_ERR_INVALID_ARG);
+  const int64_t kb = K / 2, ks = K / 16;
+  const uint4* src = reinterpret_cast<const uint4*>(codes + (ok ? v : 0) * kb);
+  uint4* dst = reinterpret_cast<uint4*>(codes_out + j * kb);
+  for (int64_t q = lane; q < kb / 16; q += 32) dst[q] = ok ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t q = lane; q < ks; q += 32) scales_out[j * ks + q] = ok ? scales[v * ks + q] : 0;
 }
 
 constexpr size_t kAlign = 256;
@@ -110,10 +130,13 @@ DenseWs carve_dense(void* base, int64_t M, int64_t N, int64_t K, bool argmax) {
   size_t off = 0;
   char* b = static_cast<char*>(base);
   if (argmax) {
+    // keys and completion counter, contiguous: the prep kernel zeroes them as 32-bit words
     w.keys = reinterpret_cast<unsigned long long*>(b + off);
     off += align_up(GV_MCHUNK * sizeof(unsigned long long));
     w.counter = reinterpret_cast<unsigned int*>(b + off);
     off += kAlign;
+    w.tile_counters = reinterpret_cast<unsigned int*>(w.keys);
+    w.n_tile_counters = static_cast<int>(off / sizeof(unsigned int));
   }
   w.pexp = reinterpret_cast<int*>(b + off);
   off += align_up(static_cast<size_t>(chunks) * GV_MCHUNK * sizeof(int));
@@ -198,14 +221,57 @@ int launch_gemm_w4a16(const uint16_t* X, int64_t M, const nvfp4_tensor_t& W, uin
   return launch_skinny_nt<SK_PLAIN>(nt, p, grid, stream);
 }
 
+int launch_gather_rows(const nvfp4_tensor_t& W, const int32_t* idx, int64_t n_idx, uint8_t* codes_out,
+                       uint8_t* scales_out, cudaStream_t stream) {
+  constexpr int kWarps = 8;
+  const int64_t blocks = ceil_div(n_idx, kWarps);
+  gather_rows_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(
+      W.codes, W.scales, W.rows, W.K, idx, n_idx, codes_out, scales_out, device_status_ptr());
+  return from_cuda(cudaGetLastError());
+}
+
+// GEMV + argmax over every row of W (consecutive rows through 2-D TMA boxes);
+// row j is reported as ids[j] (j when ids is null).
+int launch_gemv_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, const int32_t* ids,
+                       int32_t* out_ids, float* out_logit, void* ws, cudaStream_t stream) {
+  const int64_t K = W.K;
+  const DenseWs w = carve_dense(ws, M, 0, K, true);   // keys and counter zeroed by the prep kernel
+  const int nt = static_cast<int>(ceil_div(M, 8));
+  int rc = prep_dense(H, M, K, nt, w, stream);
+  if (rc != NVFP4_OK) return rc;
+  CUtensorMap mc, ms;
+  rc = make_tmap_2d_u8(&mc, W.codes, K / 2, W.rows, K / 2, 128, GV_ROWS, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != NVFP4_OK) return rc;
+  rc = make_tmap_2d_u8(&ms, W.scales, K / 16, W.rows, K / 16, 16, GV_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != NVFP4_OK) return rc;
+  TmaSkinnyParams q{};
+  q.s_t = W.s_t;
+  q.K = K;
+  q.n_rows = W.rows;
+  q.xfrag = w.xfrag;
+  q.pexp = w.pexp;
+  q.M = M;
+  q.split = 1;
+  q.status = device_status_ptr();
+  q.idx = ids;
+  q.keys = w.keys;
+  q.counter = w.counter;
+  q.out_ids = out_ids;
+  q.out_logit = out_logit;
+  const dim3 grid(1, static_cast<unsigned>(ceil_div(W.rows, GV_ROWS)), 1);
+  switch (nt) {
+    case 1: return launch_tma_argmax_nt<1, false>(q, mc, ms, grid, stream);
+    case 2: return launch_tma_argmax_nt<2, false>(q, mc, ms, grid, stream);
+    case 3: return launch_tma_argmax_nt<3, false>(q, mc, ms, grid, stream);
+    default: return launch_tma_argmax_nt<4, false>(q, mc, ms, grid, stream);
+  }
+}
+
 int launch_gather_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, const int32_t* idx,
                          int64_t n_idx, int32_t* out_ids, float* out_logit, void* ws, cudaStream_t stream) {
   const int64_t K = W.K;
   const DenseWs w = carve_dense(ws, M, 0, K, true);
-  // keys and the completion counter start at zero on every call
-  if (cudaMemsetAsync(w.keys, 0, reinterpret_cast<char*>(w.pexp) - reinterpret_cast<char*>(w.keys), stream) !=
-      cudaSuccess)
-    return NVFP4_ERR_CUDA;
+  // keys and the completion counter start at zero on every call: the prep kernel zeroes them
   const int nt = static_cast<int>(ceil_div(M, 8));
   int rc = prep_dense(H, M, K, nt, w, stream);
   if (rc != NVFP4_OK) return rc;

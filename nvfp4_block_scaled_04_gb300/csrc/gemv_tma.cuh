@@ -108,9 +108,12 @@ NVFP4_DEV uint4 lds_v4(uint32_t saddr) {
 // One K-iteration (128 K) of a stage: the warp's MT m-tiles of 16 weight rows
 // (row group grp) against NT n-tiles of 8 tokens; j selects the iteration
 // within the stage (codes at 16-byte chunks 4j..4j+3 of each 128-byte row,
-// scales at bytes 8j..8j+7, activation fragments at j * NT * 2048).
+// scales at bytes 8j..8j+7, activation fragments at j * NT * 2048). Only the
+// first nt_active n-tiles hold tokens (a partly filled chunk, e.g. an expert
+// with few routed rows); the MMAs of the others are skipped.
 template <int NT, int MT, bool GATHERED = false>
-NVFP4_DEV void gt_mma_iteration(uint32_t stage, int j, int grp, int sw, int t, int lane, float (&acc)[MT][NT][4]) {
+NVFP4_DEV void gt_mma_iteration(uint32_t stage, int j, int grp, int sw, int t, int lane, int nt_active,
+                                float (&acc)[MT][NT][4]) {
   constexpr int SC = GATHERED ? GT_SCALES_GATHERED : GT_SCALES;
   const uint32_t phys = static_cast<uint32_t>(((4 * j + t) ^ sw) << 4);
   uint32_t wa[MT][4], wb[MT][4], sa[MT][2], sb[MT][2];
@@ -145,11 +148,13 @@ NVFP4_DEV void gt_mma_iteration(uint32_t stage, int j, int grp, int sw, int t, i
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const uint4 bx = lds_v4(xs + (nt * 4 + w) * 512);
+      if (nt < nt_active) {
+        const uint4 bx = lds_v4(xs + (nt * 4 + w) * 512);
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        mma_f16_16816(acc[mt][nt], A0[mt], bx.x, bx.y);
-        mma_f16_16816(acc[mt][nt], A1[mt], bx.z, bx.w);
+        for (int mt = 0; mt < MT; ++mt) {
+          mma_f16_16816(acc[mt][nt], A0[mt], bx.x, bx.y);
+          mma_f16_16816(acc[mt][nt], A1[mt], bx.z, bx.w);
+        }
       }
     }
   }
@@ -347,6 +352,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
     const int sw = gt_sigma(g);               // smem row (mod 8) of MMA row g
     const int grp = warp % NGR;               // row group of this warp
     const int jk = warp / NGR;                // its K-iteration within a stage when KW == 2
+    const int nt_active = (rows_in_chunk + 7) / 8;
     for (int st = 0; st < n_st; ++st) {
       const int q = st % C::STAGES;
       if (!mbar_wait_bounded(full_bar(q), (st / C::STAGES) & 1, abort_flag, p.status)) break;
@@ -355,7 +361,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
       for (int jj = 0; jj < 3 - KW; ++jj) {
         const int j = KW == 2 ? jk : jj;
         if (it0 + 2LL * st + j < it_end) {
-          gt_mma_iteration<NT, MT, GATHERED>(stage, j, grp, sw, t, lane, acc);
+          gt_mma_iteration<NT, MT, GATHERED>(stage, j, grp, sw, t, lane, nt_active, acc);
         }
       }
       __syncwarp();
@@ -393,30 +399,55 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
   const float st = p.s_t[expert];
   if (S == 1) {
     const int width = (MODE == SK_MOE_GATEUP) ? 64 : GV_ROWS;
-    for (int e = tid; e < rows_in_chunk * width; e += NTHR) {
-      const int tok = e / width;
-      const int r = e % width;
-      const float v = psum(tok, r);
-      const float mul = ldexpf(st, pexp_s[tok]);
-      if (MODE == SK_PLAIN) {
-        const int64_t n = row_tile * GV_ROWS + r;
-        if (n < p.n_rows) p.Y[(row_base + tok) * p.n_rows + n] = static_cast<uint16_t>(f32_to_bf16_bits(v * mul));
-      } else if (MODE == SK_ARGMAX) {
-        // key: logit order first, then the lower vocabulary id
-        const int64_t j = row_tile * GV_ROWS + r;
-        if (j < p.n_rows) {
-          const uint32_t vid = p.idx ? static_cast<uint32_t>(p.idx[j]) : static_cast<uint32_t>(j);
-          atomicMax(&kbest[tok],
-                    (static_cast<unsigned long long>(float_order_key(v * mul)) << 32) | (0xFFFFFFFFu - vid));
+    // ARGMAX: the loop runs warp-uniformly over whole rounds of NTHR, so each
+    // round's keys can meet in a warp maximum before one shared atomic per
+    // warp and token (a 128-byte row of outputs belongs to one token)
+    const int n_out = rows_in_chunk * width;
+    const int n_loop = MODE == SK_ARGMAX ? (n_out + NTHR - 1) / NTHR * NTHR : n_out;
+    for (int e = tid; e < n_loop; e += NTHR) {
+      unsigned long long key = 0ull;
+      int key_tok = -1;
+      if (e < n_out) {
+        const int tok = e / width;
+        const int r = e % width;
+        const float v = psum(tok, r);
+        const float mul = ldexpf(st, pexp_s[tok]);
+        if (MODE == SK_PLAIN) {
+          const int64_t n = row_tile * GV_ROWS + r;
+          if (n < p.n_rows) p.Y[(row_base + tok) * p.n_rows + n] = static_cast<uint16_t>(f32_to_bf16_bits(v * mul));
+        } else if (MODE == SK_ARGMAX) {
+          // key: logit order first, then the lower vocabulary id
+          const int64_t j = row_tile * GV_ROWS + r;
+          if (j < p.n_rows) {
+            const uint32_t vid = p.idx ? static_cast<uint32_t>(p.idx[j]) : static_cast<uint32_t>(j);
+            key = (static_cast<unsigned long long>(float_order_key(v * mul)) << 32) | (0xFFFFFFFFu - vid);
+          }
+          key_tok = tok;   // set for rows past the end too: the groups below follow the output index
+        } else if (MODE == SK_MOE_GATEUP) {
+          const float gg = v * mul;
+          const float uu = psum(tok, 64 + r) * mul;
+          const float hh = gg / (1.0f + expf(-gg)) * uu;
+          p.h_out[(row_base + tok) * p.inter + row_tile * 64 + r] = static_cast<uint16_t>(f32_to_bf16_bits(hh));
+        } else {
+          const int64_t c = row_tile * GV_ROWS + r;
+          if (c < p.hidden) p.y_out[(row_base + tok) * p.hidden + c] = v * mul;
         }
-      } else if (MODE == SK_MOE_GATEUP) {
-        const float gg = v * mul;
-        const float uu = psum(tok, 64 + r) * mul;
-        const float hh = gg / (1.0f + expf(-gg)) * uu;
-        p.h_out[(row_base + tok) * p.inter + row_tile * 64 + r] = static_cast<uint16_t>(f32_to_bf16_bits(hh));
-      } else {
-        const int64_t c = row_tile * GV_ROWS + r;
-        if (c < p.hidden) p.y_out[(row_base + tok) * p.hidden + c] = v * mul;
+      }
+      if (MODE == SK_ARGMAX) {
+        // lanes of a warp cover consecutive outputs: one or two tokens per warp
+        // and round (a row of outputs is 128 wide), then lanes past the end
+        const int tok_lo = __shfl_sync(0xffffffffu, key_tok, 0);
+#pragma unroll
+        for (int side = 0; side < 2; ++side) {
+          unsigned long long k = (side == 0) == (key_tok == tok_lo) ? key : 0ull;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
+            k = other > k ? other : k;
+          }
+          const int kt = side == 0 ? tok_lo : __shfl_sync(0xffffffffu, key_tok, 31);
+          if (lane == 0 && kt >= 0 && k != 0ull && (side == 0 || kt != tok_lo)) atomicMax(&kbest[kt], k);
+        }
       }
     }
     if (MODE == SK_ARGMAX) {

@@ -83,6 +83,10 @@ int launch_gemm_w4a16(const uint16_t* X, int64_t M, const nvfp4_tensor_t& W, uin
                       cudaStream_t stream);
 int launch_gather_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, const int32_t* idx,
                          int64_t n_idx, int32_t* out_ids, float* out_logit, void* ws, cudaStream_t stream);
+int launch_gather_rows(const nvfp4_tensor_t& W, const int32_t* idx, int64_t n_idx, uint8_t* codes_out,
+                       uint8_t* scales_out, cudaStream_t stream);
+int launch_gemv_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, const int32_t* ids,
+                       int32_t* out_ids, float* out_logit, void* ws, cudaStream_t stream);
 
 // ---- moe.cu
 int launch_moe_route(const float* logits, int64_t T, int E, int topk, int32_t* ids, float* weights,

@@ -108,3 +108,16 @@ def test_validation_rejects_before_launch(nv):
     W2 = nv.CTensor(0x30000, 0x40000, 0x50000, 128, 256, 3, 0)                      # batch mismatch
     assert L.nvfp4_grouped_gemm(_fake(), 4, 2, _fake(), _fake(), W13, W2, _fake(), ws, 1 << 30, None) == -1
     assert L.nvfp4_selftest_bounded_wait(0, None) == -1
+
+
+def test_row_gather_and_compact_argmax_validate_arguments(nv):
+    L = nv.lib()
+    ws = _fake()
+    W = nv.CTensor(0x1000, 0x2000, 0x3000, 64, 256, 1, 0)
+    assert L.nvfp4_gather_rows(W, None, 4, _fake(), _fake(), None) == -1             # no index
+    Wk = nv.CTensor(0x1000, 0x2000, 0x3000, 64, 48, 1, 0)
+    assert L.nvfp4_gather_rows(Wk, _fake(), 4, _fake(), _fake(), None) == -2         # K % 32
+    assert L.nvfp4_gemv_argmax(_fake(), 0, W, None, _fake(), None, ws, 1 << 20, None) == -1   # M
+    Wa = nv.CTensor(0x1000, 0x2000, 0x3000, 64, 384, 1, 0)
+    assert L.nvfp4_gemv_argmax(_fake(), 1, Wa, None, _fake(), None, ws, 1 << 20, None) == -2  # K % 256
+    assert L.nvfp4_gemv_argmax(_fake(), 1, W, None, _fake(), None, None, 0, None) == -5       # workspace

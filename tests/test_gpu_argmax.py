@@ -73,6 +73,12 @@ def _head():
     return w, idx, nv().quantize(w.to(DEV)), st, O.quantize(w.numpy()[idx.numpy()], s_t=st)
 
 
+@functools.lru_cache(maxsize=1)
+def _compact():
+    _, idx, qw, _, _ = _head()
+    return nv().gather_rows(qw, idx.to(DEV))
+
+
 @pytest.mark.parametrize("M", [1, 4, 8])
 def test_draft_head_config(M):
     """248,320 x 5120 head, 32,768-id mask, 3 draft steps: the masked argmax
@@ -88,14 +94,16 @@ def test_draft_head_config(M):
         logits, _ = O.gather_logits(h.float().numpy(), wq_masked, None)
         omax = logits.max(axis=1)
         margin = O.top2_margin(logits)
+        # the same head as a compact prepacked copy of the masked rows
+        ids_c, logit_c = m.gemv_argmax(h.to(DEV), _compact(), idx.to(DEV))
         for r in range(M):
-            got = int(ids[r])
-            assert got in set(idx_np.tolist())
-            pos = int(np.nonzero(idx_np == got)[0][0])
-            rms = np.sqrt(np.mean(logits[r] ** 2))
-            if margin[r] > TOL:
-                assert logits[r][pos] == omax[r]
-            assert abs(float(logit[r]) - omax[r]) <= TOL * rms
+            for got, lg in ((int(ids[r]), float(logit[r])), (int(ids_c[r]), float(logit_c[r]))):
+                assert got in set(idx_np.tolist())
+                pos = int(np.nonzero(idx_np == got)[0][0])
+                rms = np.sqrt(np.mean(logits[r] ** 2))
+                if margin[r] > TOL:
+                    assert logits[r][pos] == omax[r]
+                assert abs(lg - omax[r]) <= TOL * rms
     # full vocabulary: the winner's oracle logit matches and no sampled row beats it
     h = synth.draft_hidden(M, 0)
     ids, logit = m.gather_gemv_argmax(h.to(DEV), qw, None)
@@ -106,3 +114,45 @@ def test_draft_head_config(M):
         rms = np.sqrt(np.mean(lg ** 2))
         assert abs(lg[0, -1] - float(logit[r])) <= TOL * rms
         assert lg[0].max() <= float(logit[r]) + TOL * rms
+
+
+def test_gather_rows_matches_the_oracles_rows_byte_for_byte():
+    m = nv()
+    V, K = 2000, 512
+    w = synth.normal_f32((V, K), 0.02, seed=51)
+    idx = synth.permutation_prefix(V, 333, seed=52)
+    sub = m.gather_rows(m.quantize(w.to(DEV)), idx.to(DEV))
+    ref = O.quantize(w.numpy()[idx.numpy()], s_t=O.tensor_scale(w.numpy()))
+    assert np.array_equal(sub.codes.cpu().numpy(), ref.codes)
+    assert np.array_equal(sub.scales.cpu().numpy().reshape(ref.scales.shape), ref.scales)
+
+
+@pytest.mark.parametrize("M", [1, 5, 8, 13, 32])
+def test_gemv_argmax_on_compact_rows_equals_masked_head(M):
+    """The compact copy of the masked rows with the mask as id map gives the
+    masked head's answer (checked against the oracle as well)."""
+    m = nv()
+    V, K = 4000, 512
+    w = synth.normal_f32((V, K), 0.02, seed=61)
+    idx = synth.permutation_prefix(V, 1000, seed=62)
+    h = synth.normal_bf16((M, K), seed=63 + M)
+    qw = m.quantize(w.to(DEV))
+    ids, logit = m.gemv_argmax(h.to(DEV), m.gather_rows(qw, idx.to(DEV)), idx.to(DEV))
+    check_against_oracle(ids.cpu().numpy(), logit.cpu().numpy(), h.float().numpy(), O.quantize(w.numpy()),
+                         idx.numpy())
+    ids_g, _ = m.gather_gemv_argmax(h.to(DEV), qw, idx.to(DEV))
+    _, _, logits = O.gather_gemv_argmax(h.float().numpy(), O.quantize(w.numpy()), idx.numpy())
+    margin = O.top2_margin(logits)
+    for r in range(M):
+        if margin[r] > TOL:
+            assert int(ids[r]) == int(ids_g[r])
+
+
+def test_gather_rows_out_of_range_index_is_reported():
+    m = nv()
+    qw = m.quantize(synth.normal_f32((64, 256), 0.02, seed=71).to(DEV))
+    idx = torch.tensor([3, 64, 5], dtype=torch.int32, device=DEV)
+    m.read_device_status()   # clear
+    sub = m.gather_rows(qw, idx)
+    assert m.read_device_status() == m.ERR_INVALID_ARG
+    assert int(sub.codes[1].abs().sum()) == 0 and torch.equal(sub.codes[0], qw.codes[3])
