@@ -3,7 +3,8 @@
 // NVFP4 mixture-of-experts kernel):
 //   route:    top-k of softmax(router logits), ties to the lower expert id
 //   plan:     group the T*k routed rows by expert, each expert padded to a
-//             multiple of 32 rows (one token chunk of the skinny kernel)
+//             multiple of 32 rows (one token chunk of the skinny kernel), in
+//             one single-CTA kernel
 //   gate/up:  [g; u] = x @ W13_e^T, h = bf16(silu(g) * u)
 //   down:     y = h @ W2_e^T, fp32
 // (both on the TMA-fed skinny kernel when K is a multiple of 256, else on the
@@ -61,8 +62,6 @@ __global__ void route_kernel(const float* logits, int64_t T, int E, int topk, in
 }
 
 struct MoeWs {
-  int* counts;        // [E]
-  int* cursor;        // [E]
   int* chunk_count;   // [1]
   int* poff;          // [E]
   int* chunk_expert;  // [max_chunks]
@@ -75,7 +74,6 @@ struct MoeWs {
   uint16_t* hbuf;     // [padded rows][I] bf16
   uint4* xfrag2;      // h, K = I
   float* ybuf;        // [padded rows][H] fp32
-  size_t zero_bytes;  // counts + cursor
   size_t bytes;
   int64_t max_chunks;
 };
@@ -92,9 +90,6 @@ MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
     off += align_up(bytes);
     return p;
   };
-  w.counts = reinterpret_cast<int*>(take(E * sizeof(int)));
-  w.cursor = reinterpret_cast<int*>(take(E * sizeof(int)));
-  w.zero_bytes = off;
   w.chunk_count = reinterpret_cast<int*>(take(sizeof(int)));
   w.poff = reinterpret_cast<int*>(take(E * sizeof(int)));
   w.chunk_expert = reinterpret_cast<int*>(take(w.max_chunks * sizeof(int)));
@@ -111,59 +106,59 @@ MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
   return w;
 }
 
-__global__ void count_kernel(const int32_t* ids, int64_t R, int E, int* counts) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i < R) {
-    const int e = ids[i];
-    if (e >= 0 && e < E) atomicAdd(&counts[e], 1);
-  }
-}
-
-// Single CTA: padded offsets, the chunk table, and row_of = -1 everywhere.
-// The counts are staged in shared memory first, so the (serial, in-order)
-// prefix sum runs on shared-memory latency.
 constexpr int PLAN_MAX_E = 4096;
-__global__ void plan_kernel(const int* counts, int E, int* poff, int* chunk_count, int* chunk_expert,
-                            int* chunk_rows, int* row_of) {
+
+// The whole routing plan in one CTA: count the routed rows per expert (shared
+// atomics), pad each expert to a multiple of 32 rows and prefix-sum (thread
+// 0, in expert order), write the chunk table and row_of = -1, then hand out
+// each routed row's position within its expert (shared atomics again).
+// Replaces a memset and three kernels (count, plan, scatter).
+__global__ void __launch_bounds__(1024) route_plan_kernel(const int32_t* ids, int64_t R, int topk, int E, int* poff,
+                                                          int* chunk_count, int* chunk_expert, int* chunk_rows,
+                                                          int* row_of, int* pos_of) {
+  __shared__ int s_cnt[PLAN_MAX_E];
+  __shared__ int s_off[PLAN_MAX_E];
   __shared__ int s_total;
-  __shared__ int s_pad[PLAN_MAX_E];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_pad[e] = (counts[e] + GV_MCHUNK - 1) / GV_MCHUNK * GV_MCHUNK;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  for (int64_t i = threadIdx.x; i < R; i += blockDim.x) {
+    const int e = ids[i];
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     int acc = 0;
     for (int e = 0; e < E; ++e) {
-      const int n = s_pad[e];
-      s_pad[e] = acc;
-      acc += n;
+      s_off[e] = acc;
+      acc += (s_cnt[e] + GV_MCHUNK - 1) / GV_MCHUNK * GV_MCHUNK;
     }
     s_total = acc;
     *chunk_count = acc / GV_MCHUNK;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) poff[e] = s_pad[e];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int n = counts[e];
-    const int c0 = poff[e] / GV_MCHUNK;
+    poff[e] = s_off[e];
+    const int n = s_cnt[e];
+    const int c0 = s_off[e] / GV_MCHUNK;
     for (int c = 0; c * GV_MCHUNK < n; ++c) {
       chunk_expert[c0 + c] = e;
       chunk_rows[c0 + c] = min(GV_MCHUNK, n - c * GV_MCHUNK);
     }
   }
   for (int r = threadIdx.x; r < s_total; r += blockDim.x) row_of[r] = -1;
-}
-
-__global__ void scatter_kernel(const int32_t* ids, int64_t R, int topk, int E, const int* poff, int* cursor,
-                               int* row_of, int* pos_of) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= R) return;
-  const int e = ids[i];
-  if (e < 0 || e >= E) {
-    pos_of[i] = -1;
-    return;
+  __syncthreads();   // row_of = -1 before any position is written; counts reused as cursors
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  for (int64_t i = threadIdx.x; i < R; i += blockDim.x) {
+    const int e = ids[i];
+    if (e < 0 || e >= E) {
+      pos_of[i] = -1;
+      continue;
+    }
+    const int pos = s_off[e] + atomicAdd(&s_cnt[e], 1);
+    row_of[pos] = static_cast<int>(i / topk);
+    pos_of[i] = pos;
   }
-  const int pos = poff[e] + atomicAdd(&cursor[e], 1);
-  row_of[pos] = static_cast<int>(i / topk);
-  pos_of[i] = pos;
 }
 
 // One CTA per padded row (rows longer than MOE_PREP_MAX_K).
@@ -319,14 +314,11 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
   const int64_t R = T * topk;
   if (E > PLAN_MAX_E) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   const MoeWs m = carve_moe(ws, T, H, I, E, topk);
-  if (cudaMemsetAsync(m.counts, 0, m.zero_bytes, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
-  const unsigned gr = static_cast<unsigned>(ceil_div(R, 256));
-  count_kernel<<<gr, 256, 0, stream>>>(ids, R, static_cast<int>(E), m.counts);
-  plan_kernel<<<1, 1024, 0, stream>>>(m.counts, static_cast<int>(E), m.poff, m.chunk_count, m.chunk_expert,
-                                      m.chunk_rows, m.row_of);
-  scatter_kernel<<<gr, 256, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.cursor, m.row_of,
-                                         m.pos_of);
-  int rc = prep_moe(X, H, true, m, m.xfrag1, m.pexp1, stream);
+  route_plan_kernel<<<1, 1024, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.chunk_count,
+                                            m.chunk_expert, m.chunk_rows, m.row_of, m.pos_of);
+  int rc = from_cuda(cudaGetLastError());
+  if (rc != NVFP4_OK) return rc;
+  rc = prep_moe(X, H, true, m, m.xfrag1, m.pexp1, stream);
   if (rc != NVFP4_OK) return rc;
 
   if (H % 256 == 0 && I % 256 == 0) {

@@ -257,10 +257,21 @@ int launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t
     }
   }
   if (rows * ((K / 16 + 63) / 64) >= (1LL << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  const int g = grid_for(n8 > 0 ? n8 : 1, Q_THREADS);
-#define NVFP4_Q(T, L)                                                                                  \
-  quantize_kernel<T, L><<<g, Q_THREADS, 0, stream>>>(static_cast<const T*>(x), rows, K, codes, scales, \
-                                                     amax, s_t, s_t_mode, cols4)
+  // one full wave of resident blocks (the chunks are walked with a grid
+  // stride): a grid of 8 blocks per SM at 6 resident left a quarter of the
+  // work to a second, partial wave
+  const int g_max = grid_for(n8 > 0 ? n8 : 1, Q_THREADS);
+#define NVFP4_Q(T, L)                                                                                         \
+  do {                                                                                                        \
+    int per_sm = 0;                                                                                           \
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_kernel<T, L>, Q_THREADS, 0) !=        \
+            cudaSuccess ||                                                                                    \
+        per_sm < 1)                                                                                           \
+      per_sm = 1;                                                                                             \
+    const int g = g_max < per_sm * sm_count() ? g_max : per_sm * sm_count();                                  \
+    quantize_kernel<T, L><<<g, Q_THREADS, 0, stream>>>(static_cast<const T*>(x), rows, K, codes, scales, amax, \
+                                                       s_t, s_t_mode, cols4);                                 \
+  } while (0)
   if (x_dtype == NVFP4_DTYPE_BF16) {
     if (scale_layout == NVFP4_SCALES_MMA) NVFP4_Q(uint16_t, NVFP4_SCALES_MMA);
     else NVFP4_Q(uint16_t, NVFP4_SCALES_ROWMAJOR);
