@@ -432,6 +432,18 @@ def _oracle_weights():
     return _ORACLE_W
 
 
+_ORACLE_X = {}
+
+
+def _oracle_activation(M, K):
+    """The step's bf16 activations as fp32 on the host (drawn once; drawing
+    them is not the oracle's work)."""
+    import synth
+    if (M, K) not in _ORACLE_X:
+        _ORACLE_X[(M, K)] = synth.decode_activation(M, K).float().numpy()
+    return _ORACLE_X[(M, K)]
+
+
 def oracle_decode_sample(budget_s, rows_per_call=None):
     """The oracle's W4A16 decode on a bounded sample: for each of the eight
     calls, `rows_per_call` weight rows (quantised by the oracle with the full
@@ -441,17 +453,16 @@ def oracle_decode_sample(budget_s, rows_per_call=None):
     import numpy as np
 
     import oracle as O
-    import synth
     mats = _oracle_weights()
     if rows_per_call is None:
         _, t_trial, _ = oracle_decode_sample(budget_s, 16)
-        rows_per_call = int(max(16, min(4096, 16 * budget_s / max(t_trial, 1e-3))))
+        rows_per_call = int(max(1, min(4096, 16 * budget_s / max(t_trial, 1e-3))))
     rng = np.random.default_rng(0)
     total_b, t_total = 0, 0.0
     for M in DECODE_M:
         for name, N, K in DECODE_MATS:
             w, st = mats[name]
-            x = synth.decode_activation(M, K).float().numpy()
+            x = _oracle_activation(M, K)
             r = np.sort(rng.choice(N, min(rows_per_call, N), replace=False))
             t0 = time.perf_counter()
             q = O.quantize(w[r], s_t=st)
@@ -557,7 +568,8 @@ def run_reference(args):
     world, rank, _ = dist_info()
     if rank != 0:
         return
-    budget = max(1.0, min(8.0, 120.0 / max(1, args.steps + args.warmup + 1)))
+    # each step a sample sized so the whole run stays within a few minutes
+    budget = min(8.0, 120.0 / max(1, args.steps + args.warmup + 1))
     _, _, rows = oracle_decode_sample(budget)
     for _ in range(args.warmup):
         oracle_decode_sample(budget, rows)
