@@ -295,18 +295,36 @@ class Decode:
 
 
 def e2e_graph(dec):
-    """One step through the public API with pinned host buffers: copy each
-    call's activations host -> device, run it, copy its output device -> host."""
+    """One step through the public API with pinned host buffers: every call's
+    activations are copied host -> device and its output device -> host.
+    The copies run on a second stream, as a serving loop would issue them: all
+    uploads at the start of the step, each output read back as soon as its
+    call has finished, while the next calls compute."""
     import torch
     hx = {k: v.cpu().pin_memory() for k, v in dec.x.items()}
     hy = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in dec.y.items()}
     calls = dec.calls()
+    copies = torch.cuda.Stream()
 
     def fn():
+        main = torch.cuda.current_stream()
+        copies.wait_stream(main)
+        uploaded = []
+        with torch.cuda.stream(copies):
+            for M, name, _, _ in calls:
+                dec.x[(M, name)].copy_(hx[(M, name)], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copies)
+                uploaded.append(ev)
         for j, (M, name, _, _) in enumerate(calls):
-            dec.x[(M, name)].copy_(hx[(M, name)], non_blocking=True)
+            main.wait_event(uploaded[j])
             dec.call(M, name, j % REPLICAS)
-            hy[(M, name)].copy_(dec.y[(M, name)], non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(main)
+            copies.wait_event(done)
+            with torch.cuda.stream(copies):
+                hy[(M, name)].copy_(dec.y[(M, name)], non_blocking=True)
+        main.wait_stream(copies)
     h2d = sum(v.numel() * v.element_size() for v in hx.values())
     d2h = sum(v.numel() * v.element_size() for v in hy.values())
     return capture(fn), h2d, d2h
