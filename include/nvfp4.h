@@ -249,9 +249,10 @@ size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t c, int64_t e, 
 /* Human-readable name of a status code (static storage). */
 const char* nvfp4_status_string(int status);
 
-/* Reads and clears the device status word that bounded on-device waits set
- * when they give up (synchronises `stream`). *out = NVFP4_OK or
- * NVFP4_ERR_TIMEOUT. */
+/* Reads and clears the device status word (synchronises `stream`). Bounded
+ * on-device waits that give up set NVFP4_ERR_TIMEOUT; nvfp4_gather_rows sets
+ * NVFP4_ERR_INVALID_ARG for an index outside the matrix. *out = NVFP4_OK or
+ * the last status set. */
 int nvfp4_read_device_status(int* out, nvfp4_stream_t stream);
 
 /* Self-test of the bounded-wait machinery: launches one CTA that waits on an
