@@ -321,6 +321,12 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
           tma_load_2d(stage + GT_CODES / 2, &map_codes, xc, y_b, full_bar(q));
           tma_load_2d(stage + GT_CODES, &map_scales, xs, y_a, full_bar(q));
           tma_load_2d(stage + GT_CODES + GT_SCALES / 2, &map_scales, xs, y_b, full_bar(q));
+        } else if (MODE == SK_PLAIN || MODE == SK_ARGMAX) {
+          // every weight byte is read once per call: evict it first (measured:
+          // decode step 183 -> 177 us); the routed experts re-read theirs
+          const uint64_t pol = l2_policy_evict_first();
+          tma_load_2d_hint(stage, &map_codes, xc, y_a, full_bar(q), pol);
+          tma_load_2d_hint(stage + GT_CODES, &map_scales, xs, y_a, full_bar(q), pol);
         } else {
           tma_load_2d(stage, &map_codes, xc, y_a, full_bar(q));
           tma_load_2d(stage + GT_CODES, &map_scales, xs, y_a, full_bar(q));

@@ -86,6 +86,23 @@ NVFP4_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t
                : "memory");
 }
 
+// L2 eviction priority for data a kernel reads exactly once (streamed
+// weights): evict_first keeps it from displacing what L2 holds for others.
+NVFP4_DEV uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_2d with an L2 cache policy (from createpolicy).
+NVFP4_DEV void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05): start >> 4 at bit 0, leading
 // byte offset >> 4 at bit 16, stride byte offset >> 4 at bit 32, version 1
 // at bit 46, layout (swizzle mode) at bit 61.
