@@ -77,6 +77,7 @@ struct TmaSkinnyParams {
   int* status;
   float* partials;             // split-K > 1: [tile][split][32 tokens][128 rows] fp32
   unsigned int* counters;      // split-K > 1: one arrival counter per tile, zeroed by the prep kernel
+  int weights_once;            // MoE: each weight byte is read once per call (evict-first L2 policy)
   // ARGMAX (split 1): candidate j is weight row idx[j] (row j when idx is null)
   const int32_t* idx;
   unsigned long long* keys;    // [M] best (logit order key, ~id) so far, zero on entry
@@ -316,14 +317,22 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
         mbar_arrive_expect_tx(full_bar(q), bytes);
         const int xc = static_cast<int>((it0 + 2LL * st) * 64);
         const int xs = static_cast<int>((it0 + 2LL * st) * 8);
-        if (MODE == SK_MOE_GATEUP) {
+        // a weight byte read once per call is evicted from L2 first (measured:
+        // decode step 183 -> 177 us, MoE layer at 256 tokens 173 -> 167 us);
+        // routed experts with several token chunks re-read theirs
+        const bool once = MODE == SK_PLAIN || MODE == SK_ARGMAX || p.weights_once;
+        if (MODE == SK_MOE_GATEUP && once) {
+          const uint64_t pol = l2_policy_evict_first();
+          tma_load_2d_hint(stage, &map_codes, xc, y_a, full_bar(q), pol);
+          tma_load_2d_hint(stage + GT_CODES / 2, &map_codes, xc, y_b, full_bar(q), pol);
+          tma_load_2d_hint(stage + GT_CODES, &map_scales, xs, y_a, full_bar(q), pol);
+          tma_load_2d_hint(stage + GT_CODES + GT_SCALES / 2, &map_scales, xs, y_b, full_bar(q), pol);
+        } else if (MODE == SK_MOE_GATEUP) {
           tma_load_2d(stage, &map_codes, xc, y_a, full_bar(q));
           tma_load_2d(stage + GT_CODES / 2, &map_codes, xc, y_b, full_bar(q));
           tma_load_2d(stage + GT_CODES, &map_scales, xs, y_a, full_bar(q));
           tma_load_2d(stage + GT_CODES + GT_SCALES / 2, &map_scales, xs, y_b, full_bar(q));
-        } else if (MODE == SK_PLAIN || MODE == SK_ARGMAX) {
-          // every weight byte is read once per call: evict it first (measured:
-          // decode step 183 -> 177 us); the routed experts re-read theirs
+        } else if (once) {
           const uint64_t pol = l2_policy_evict_first();
           tma_load_2d_hint(stage, &map_codes, xc, y_a, full_bar(q), pol);
           tma_load_2d_hint(stage + GT_CODES, &map_scales, xs, y_a, full_bar(q), pol);

@@ -336,6 +336,7 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
     p.rows_per_expert = 2 * I;
     p.h_out = m.hbuf;
     p.status = device_status_ptr();
+    p.weights_once = R <= GV_MCHUNK * E;   // about one token chunk per expert
     rc = launch_moe_tma<SK_MOE_GATEUP>(W13, 64, p,
                                        dim3(static_cast<unsigned>(m.max_chunks), static_cast<unsigned>(I / 64)),
                                        stream);
