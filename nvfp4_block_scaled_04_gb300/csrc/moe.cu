@@ -8,7 +8,8 @@
 //   gate/up:  [g; u] = x @ W13_e^T, h = bf16(silu(g) * u)
 //   down:     y = h @ W2_e^T, fp32
 // (both on the TMA-fed skinny kernel when K is a multiple of 256, else on the
-// register-fed one)
+// register-fed one; with at least XT_MIN_ROWS_PER_EXPERT routed rows per
+// expert on average, on the tensor cores instead: moe_tc.cuh)
 //   combine:  out[t] = bf16(sum_j w[t][j] * y[pos(t, j)]), slots in order
 // The order in which routed rows land inside an expert's group comes from
 // atomics, but every row's arithmetic is independent of its position, so the
@@ -16,6 +17,7 @@
 #include "gemv_core.cuh"
 #include "gemv_tma.cuh"
 #include "launch.h"
+#include "moe_tc.cuh"
 
 namespace nvfp4 {
 
@@ -66,6 +68,10 @@ struct MoeWs {
   int* poff;          // [E]
   int* chunk_expert;  // [max_chunks]
   int* chunk_rows;    // [max_chunks]
+  int* tile_count;    // [1]  tensor-core tiles: up to XT_NMAX rows of one expert
+  int* tile_expert;   // [max_tiles]
+  int* tile_row0;     // [max_tiles]
+  int* tile_rows;     // [max_tiles]
   int* row_of;        // [padded rows] token id or -1
   int* pos_of;        // [T*k]
   int* pexp1;         // [padded rows]
@@ -76,12 +82,14 @@ struct MoeWs {
   float* ybuf;        // [padded rows][H] fp32
   size_t bytes;
   int64_t max_chunks;
+  int64_t max_tiles;
 };
 
 MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
   MoeWs w{};
   const int64_t R = T * topk;
   w.max_chunks = ceil_div(R, GV_MCHUNK) + E;
+  w.max_tiles = ceil_div(R, XT_NMAX) + E;
   const int64_t rows = w.max_chunks * GV_MCHUNK;
   char* b = static_cast<char*>(base);
   size_t off = 0;
@@ -94,6 +102,10 @@ MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
   w.poff = reinterpret_cast<int*>(take(E * sizeof(int)));
   w.chunk_expert = reinterpret_cast<int*>(take(w.max_chunks * sizeof(int)));
   w.chunk_rows = reinterpret_cast<int*>(take(w.max_chunks * sizeof(int)));
+  w.tile_count = reinterpret_cast<int*>(take(sizeof(int)));
+  w.tile_expert = reinterpret_cast<int*>(take(w.max_tiles * sizeof(int)));
+  w.tile_row0 = reinterpret_cast<int*>(take(w.max_tiles * sizeof(int)));
+  w.tile_rows = reinterpret_cast<int*>(take(w.max_tiles * sizeof(int)));
   w.row_of = reinterpret_cast<int*>(take(rows * sizeof(int)));
   w.pos_of = reinterpret_cast<int*>(take(R * sizeof(int)));
   w.pexp1 = reinterpret_cast<int*>(take(rows * sizeof(int)));
@@ -107,15 +119,19 @@ MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
 }
 
 constexpr int PLAN_MAX_E = 4096;
+// average routed rows per expert from which the expert GEMMs run on the tensor cores
+constexpr int XT_MIN_ROWS_PER_EXPERT = 64;
 
 // The whole routing plan in one CTA: count the routed rows per expert (shared
 // atomics), pad each expert to a multiple of 32 rows and prefix-sum (thread
-// 0, in expert order), write the chunk table and row_of = -1, then hand out
-// each routed row's position within its expert (shared atomics again).
-// Replaces a memset and three kernels (count, plan, scatter).
+// 0, in expert order, also writing the tensor-core tile table: each expert's
+// rows in tiles of up to XT_NMAX), write the chunk table and row_of = -1,
+// then hand out each routed row's position within its expert (shared atomics
+// again). Replaces a memset and three kernels (count, plan, scatter).
 __global__ void __launch_bounds__(1024) route_plan_kernel(const int32_t* ids, int64_t R, int topk, int E, int* poff,
                                                           int* chunk_count, int* chunk_expert, int* chunk_rows,
-                                                          int* row_of, int* pos_of) {
+                                                          int* tile_count, int* tile_expert, int* tile_row0,
+                                                          int* tile_rows, int* row_of, int* pos_of) {
   __shared__ int s_cnt[PLAN_MAX_E];
   __shared__ int s_off[PLAN_MAX_E];
   __shared__ int s_total;
@@ -127,13 +143,19 @@ __global__ void __launch_bounds__(1024) route_plan_kernel(const int32_t* ids, in
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int acc = 0;
+    int acc = 0, tiles = 0;
     for (int e = 0; e < E; ++e) {
       s_off[e] = acc;
+      for (int r = 0; r < s_cnt[e]; r += XT_NMAX, ++tiles) {
+        tile_expert[tiles] = e;
+        tile_row0[tiles] = acc + r;
+        tile_rows[tiles] = min(XT_NMAX, s_cnt[e] - r);
+      }
       acc += (s_cnt[e] + GV_MCHUNK - 1) / GV_MCHUNK * GV_MCHUNK;
     }
     s_total = acc;
     *chunk_count = acc / GV_MCHUNK;
+    *tile_count = tiles;
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -230,6 +252,54 @@ __global__ void __launch_bounds__(MOE_PREP_WARPS * 32) xprep_moe_kernel(const ui
   }
 }
 
+// The same per-row conversion into row-major f16 rows [padded rows][K] (the
+// tensor-core path's B operand, read by TMA): one warp per padded row.
+__global__ void __launch_bounds__(MOE_PREP_WARPS * 32) xprep_moe_rows_kernel(const uint16_t* src, int64_t K,
+                                                                              bool gather, const int* row_of,
+                                                                              const int* chunk_count, uint4* xrow,
+                                                                              int* pexp) {
+  constexpr int CH = MOE_PREP_MAX_K / 8 / 32;   // 16-byte chunks per lane
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * MOE_PREP_WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= static_cast<int64_t>(*chunk_count) * GV_MCHUNK) return;
+  const int tok = row_of[r];
+  const uint16_t* s = nullptr;
+  if (tok >= 0) s = gather ? src + static_cast<int64_t>(tok) * K : src + r * K;
+  const int64_t n8 = K / 8;
+  uint4 v[CH];
+  float amax = 0.f;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int64_t q = lane + 32 * c;
+    v[c] = make_uint4(0, 0, 0, 0);
+    if (s != nullptr && q < n8) v[c] = __ldg(reinterpret_cast<const uint4*>(s) + q);
+    const uint32_t w4[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] & 0xFFFFu)));
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] >> 16)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  int p = 0;
+  if (amax > 0.f) p = min(max(ilogbf(amax) - 14, -100), 113);
+  const float mul = ldexpf(1.0f, -p);
+  if (lane == 0) pexp[r] = p;
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int64_t q = lane + 32 * c;
+    if (q < n8) {
+      uint4 o;
+      o.x = f32x2_to_f16x2(bf16_bits_to_f32(v[c].x & 0xFFFFu) * mul, bf16_bits_to_f32(v[c].x >> 16) * mul);
+      o.y = f32x2_to_f16x2(bf16_bits_to_f32(v[c].y & 0xFFFFu) * mul, bf16_bits_to_f32(v[c].y >> 16) * mul);
+      o.z = f32x2_to_f16x2(bf16_bits_to_f32(v[c].z & 0xFFFFu) * mul, bf16_bits_to_f32(v[c].z >> 16) * mul);
+      o.w = f32x2_to_f16x2(bf16_bits_to_f32(v[c].w & 0xFFFFu) * mul, bf16_bits_to_f32(v[c].w >> 16) * mul);
+      xrow[r * n8 + q] = o;
+    }
+  }
+}
+
 // out[t][c] = bf16(sum_j w[t][j] * y[pos(t, j)][c]), slots in order; one
 // thread per 4 columns (H % 4 == 0), CTA (t, column block of 1024).
 __global__ void combine_kernel(const float* ybuf, const int* pos_of, const float* w, int64_t T, int topk,
@@ -285,6 +355,36 @@ int prep_moe(const uint16_t* src, int64_t K, bool gather, const MoeWs& m, uint4*
   return from_cuda(cudaGetLastError());
 }
 
+// Row-major f16 prep of the routed rows for the tensor-core path.
+int prep_moe_rows(const uint16_t* src, int64_t K, bool gather, const MoeWs& m, void* xrow, int* pexp,
+                  cudaStream_t stream) {
+  const int64_t prow = m.max_chunks * GV_MCHUNK;
+  xprep_moe_rows_kernel<<<static_cast<unsigned>(ceil_div(prow, MOE_PREP_WARPS)), MOE_PREP_WARPS * 32, 0, stream>>>(
+      src, K, gather, m.row_of, m.chunk_count, static_cast<uint4*>(xrow), pexp);
+  return from_cuda(cudaGetLastError());
+}
+
+// One expert GEMM on the tensor cores: CTA (tile, weight block), CTAs past
+// the routed tiles exit at once. xrow holds the f16 rows [padded rows][K].
+template <bool GATEUP>
+int launch_moe_tc(const nvfp4_tensor_t& W, const MoeWs& m, const void* xrow, const MoeTcParams& p,
+                  cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(W.batch) * W.rows;
+  const int64_t prow = m.max_chunks * GV_MCHUNK;
+  CUtensorMap mx, mw;
+  int rc = make_tmap_2d_u16(&mx, xrow, p.K, prow, static_cast<int64_t>(p.K) * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != NVFP4_OK) return rc;
+  rc = make_tmap_2d_u8(&mw, W.codes, W.K / 2, rows, W.K / 2, 32, GATEUP ? 64 : 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != NVFP4_OK) return rc;
+  auto k = moe_tc_kernel<GATEUP>;
+  rc = ensure_smem(k, XT_SMEM);
+  if (rc != NVFP4_OK) return rc;
+  const unsigned blocks = static_cast<unsigned>(GATEUP ? p.inter / 64 : p.hidden / 128);
+  // weight blocks along x: the CTAs of one routed-row tile run next to each other
+  return launch_ex(k, dim3(blocks, static_cast<unsigned>(m.max_tiles)), dim3(XT_THREADS), XT_SMEM, 1, false, stream,
+                   mx, mw, p);
+}
+
 int combine(const MoeWs& m, const float* w, int64_t T, int topk, int64_t H, uint16_t* out, cudaStream_t stream) {
   combine_kernel<<<dim3(static_cast<unsigned>(T), static_cast<unsigned>(ceil_div(H, 1024))), 256, 0, stream>>>(
       m.ybuf, m.pos_of, w, T, topk, H, out);
@@ -315,9 +415,48 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
   if (E > PLAN_MAX_E) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   const MoeWs m = carve_moe(ws, T, H, I, E, topk);
   route_plan_kernel<<<1, 1024, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.chunk_count,
-                                            m.chunk_expert, m.chunk_rows, m.row_of, m.pos_of);
+                                            m.chunk_expert, m.chunk_rows, m.tile_count, m.tile_expert, m.tile_row0,
+                                            m.tile_rows, m.row_of, m.pos_of);
   int rc = from_cuda(cudaGetLastError());
   if (rc != NVFP4_OK) return rc;
+
+  // Many rows per expert: the tensor cores (the f16 rows live where the
+  // fragment-order copies would).
+  if (R >= XT_MIN_ROWS_PER_EXPERT * E && m.max_tiles <= 65535 && H % 128 == 0 && I % 128 == 0 && H <= MOE_PREP_MAX_K &&
+      I <= MOE_PREP_MAX_K && ((reinterpret_cast<uintptr_t>(W13.scales) | reinterpret_cast<uintptr_t>(W2.scales)) & 3) == 0) {
+    rc = prep_moe_rows(X, H, true, m, m.xfrag1, m.pexp1, stream);
+    if (rc != NVFP4_OK) return rc;
+    MoeTcParams p{};
+    p.scales = W13.scales;
+    p.s_t = W13.s_t;
+    p.pexp = m.pexp1;
+    p.tile_count = m.tile_count;
+    p.tile_expert = m.tile_expert;
+    p.tile_row0 = m.tile_row0;
+    p.tile_rows = m.tile_rows;
+    p.K = static_cast<int>(H);
+    p.rows_per_expert = static_cast<int>(2 * I);
+    p.inter = static_cast<int>(I);
+    p.hidden = static_cast<int>(H);
+    p.h_out = m.hbuf;
+    p.status = device_status_ptr();
+    rc = launch_moe_tc<true>(W13, m, m.xfrag1, p, stream);
+    if (rc != NVFP4_OK) return rc;
+    rc = prep_moe_rows(m.hbuf, I, false, m, m.xfrag2, m.pexp2, stream);
+    if (rc != NVFP4_OK) return rc;
+    MoeTcParams q = p;
+    q.scales = W2.scales;
+    q.s_t = W2.s_t;
+    q.pexp = m.pexp2;
+    q.K = static_cast<int>(I);
+    q.rows_per_expert = static_cast<int>(H);
+    q.h_out = nullptr;
+    q.y_out = m.ybuf;
+    rc = launch_moe_tc<false>(W2, m, m.xfrag2, q, stream);
+    if (rc != NVFP4_OK) return rc;
+    return combine(m, w, T, topk, H, out, stream);
+  }
+
   rc = prep_moe(X, H, true, m, m.xfrag1, m.pexp1, stream);
   if (rc != NVFP4_OK) return rc;
 

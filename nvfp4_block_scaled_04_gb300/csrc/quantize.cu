@@ -76,39 +76,67 @@ __global__ void __launch_bounds__(Q_THREADS) amax_kernel(const T* x, int64_t n8,
   }
 }
 
-// Byte offset of block scale (row, col) in the MMA layout with `cols4`
-// (padded K/16) columns.
-NVFP4_DEV int64_t mma_scale_offset(int64_t row, int64_t col, int64_t cols4) {
-  const int64_t tile = (row >> 7) * (cols4 >> 2) + (col >> 2);
-  return tile * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (col & 3);
+// Packed fp32 pair multiply (both halves rounded to nearest even).
+NVFP4_DEV uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+NVFP4_DEV uint64_t f32_pair(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+// Four fp32 pairs (elements 2j, 2j + 1) -> eight e2m1 codes, element j in
+// nibble j (nearest even, saturating at 6, sign kept on a zero magnitude).
+NVFP4_DEV uint32_t e2m1x8_of_pairs(uint64_t p0, uint64_t p1, uint64_t p2, uint64_t p3) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .f32 a0, a1, a2, a3, a4, a5, a6, a7;\n\t"
+      "mov.b64 {a0, a1}, %1;\n\tmov.b64 {a2, a3}, %2;\n\tmov.b64 {a4, a5}, %3;\n\tmov.b64 {a6, a7}, %4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, a1, a0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, a3, a2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, a5, a4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, a7, a6;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "l"(p0), "l"(p1), "l"(p2), "l"(p3));
+  return out;
 }
 
-// Eight codes of one block half, packed: element j in nibble j. The code is
-// RNE_e2m1(fl(x / den)) with the sign of x kept on a zero magnitude; the
-// conversion instruction rounds to nearest even, saturates at 6 and keeps the
-// sign of a negative quotient that rounds to zero. The code depends only on
-// which side of the e2m1 rounding midpoints the quotient lies:
-// q~ = x * RN(1/den) is within ~2^-22 (relative) of fl(x / den), so if
-// q~ (1 - 2^-20) and q~ (1 + 2^-20) give the same codes, no midpoint lies
-// near any of the eight quotients and those are the codes of the exact
-// quotients; otherwise (ties, values at a midpoint's edge) the eight
-// quotients are formed by IEEE division.
-NVFP4_DEV uint32_t e2m1x8(const float* v, float den, float r, bool fast) {
-  if (fast) {
-    float hi[8], lo[8];
+// The sixteen codes of one block (two words, element j of each half in nibble
+// j). A code is RNE_e2m1(fl(x / den)) with the sign of x kept on a zero
+// magnitude, and depends only on which side of the e2m1 rounding midpoints
+// the quotient lies. With r = RN(1/den), rh = RN(r (1 + 2^-20)) > 1/den and
+// rl = RN(r (1 - 2^-20)) < 1/den, so RN(|x| rl) <= fl(|x| / den) <= RN(|x| rh)
+// (rounding is monotone), and the code magnitude is monotone in the value:
+// where the products with rl and rh give the same codes, those are the codes
+// of the exact quotients. Otherwise (a quotient at or next to a midpoint) the
+// sixteen quotients are formed by IEEE division.
+NVFP4_DEV uint2 e2m1x16(const float (&v)[16], float den) {
+  if (den > 1e-30f && den < 1e30f) {
+    const float r = __frcp_rn(den);
+    const float rh = __fmul_rn(r, 1.0f + 0x1p-20f), rl = __fmul_rn(r, 1.0f - 0x1p-20f);
+    const uint64_t RH = f32_pair(rh, rh), RL = f32_pair(rl, rl);
+    uint64_t ph[8], pl[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float q = __fmul_rn(v[j], r);
-      hi[j] = __fmul_rn(q, 1.0f + 0x1p-20f);
-      lo[j] = __fmul_rn(q, 1.0f - 0x1p-20f);
+    for (int e = 0; e < 8; ++e) {
+      const uint64_t xv = f32_pair(v[2 * e], v[2 * e + 1]);
+      ph[e] = mul_f32x2(xv, RH);
+      pl[e] = mul_f32x2(xv, RL);
     }
-    const uint32_t a = f32x8_to_e2m1x8(hi), b = f32x8_to_e2m1x8(lo);
-    if (a == b) return a;
+    const uint32_t h0 = e2m1x8_of_pairs(ph[0], ph[1], ph[2], ph[3]), h1 = e2m1x8_of_pairs(ph[4], ph[5], ph[6], ph[7]);
+    const uint32_t l0 = e2m1x8_of_pairs(pl[0], pl[1], pl[2], pl[3]), l1 = e2m1x8_of_pairs(pl[4], pl[5], pl[6], pl[7]);
+    if (h0 == l0 && h1 == l1) return make_uint2(h0, h1);
   }
+  uint2 out;
   float q[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(v[j], den);
-  return f32x8_to_e2m1x8(q);
+  out.x = f32x8_to_e2m1x8(q);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(v[8 + j], den);
+  out.y = f32x8_to_e2m1x8(q);
+  return out;
 }
 
 // 16-byte words of one 16-element block: 2 (bf16) or 4 (fp32).
@@ -126,8 +154,8 @@ NVFP4_DEV void unpack16<uint16_t>(const uint4 (&w)[2], float (&v)[16]) {
     const uint32_t u[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      v[8 * i + 2 * e] = bf16_bits_to_f32(u[e] & 0xFFFFu);
-      v[8 * i + 2 * e + 1] = bf16_bits_to_f32(u[e] >> 16);
+      v[8 * i + 2 * e] = __uint_as_float(u[e] << 16);
+      v[8 * i + 2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
     }
   }
 }
@@ -143,13 +171,16 @@ NVFP4_DEV void unpack16<float>(const uint4 (&w)[4], float (&v)[16]) {
 }
 
 // One thread quantises BPT blocks of 16 elements, 32 blocks apart in the row:
-// the raw words of all of them are requested before any is converted, so
-// 2 KB per warp are in flight, at up to 48 warps per SM. The block scale is formed once per block; a
-// warp covers 32 * BPT consecutive blocks of a row. Warps take these chunks
-// from the END of the tensor backwards: right after the amax pass, the tail
-// of the input is still in L2.
+// the raw words of all of them are requested before any is converted. A warp
+// covers a chunk of 32 * BPT consecutive blocks of a row; warps take chunks
+// from the END of the tensor backwards (right after the amax pass, the tail
+// of the input is still in L2), stepping by the warp count without a division
+// per step. MMA-layout scale offsets split into a row part (per chunk) and a
+// column part: byte (row, col) of the layout with `cols4` (padded K/16)
+// columns is tile * 512 + (row % 32) * 16 + ((row / 32) % 4) * 4 + col % 4,
+// tile = (row / 128) * (cols4 / 4) + col / 4.
 template <typename T, int LAYOUT>
-__global__ void __launch_bounds__(Q_THREADS, 6) quantize_kernel(const T* x, int64_t rows, int64_t K,
+__global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int64_t rows, int64_t K,
                                                                  uint8_t* codes, uint8_t* scales,
                                                                  const unsigned int* amax_bits, float* s_t,
                                                                  int mode, int64_t cols4) {
@@ -164,47 +195,50 @@ __global__ void __launch_bounds__(Q_THREADS, 6) quantize_kernel(const T* x, int6
     st = *s_t;
   }
   const float d = __fmul_rn(st, 6.0f);
-  // chunk indices fit in 32 bits (checked at launch): no 64-bit division here
+  // chunk indices fit in 32 bits (checked at launch)
   const uint32_t bpr = static_cast<uint32_t>(K / 16);
-  const uint32_t cpr = (bpr + 32 * BPT - 1) / (32 * BPT);
+  const int cpr = static_cast<int>((bpr + 32 * BPT - 1) / (32 * BPT));
   const int lane = threadIdx.x & 31;
   const int warps = static_cast<int>(gridDim.x * (blockDim.x / 32));
   const int n_chunks = static_cast<int>(rows * cpr);
-  for (int c = n_chunks - 1 - static_cast<int>(blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)); c >= 0;
-       c -= warps) {
-    const uint32_t row32 = static_cast<uint32_t>(c) / cpr;
-    const uint32_t b0 = (static_cast<uint32_t>(c) - row32 * cpr) * (32 * BPT) + lane;
-    const int64_t row = row32;
+  const int c0 = n_chunks - 1 - static_cast<int>(blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5));
+  if (c0 < 0) return;
+  int row = c0 / cpr, cc = c0 - row * cpr;
+  const int drow = warps / cpr, dcc = warps - drow * cpr;
+  const int64_t tiles_per_row = cols4 >> 2;
+  while (row >= 0) {
+    const uint32_t b0 = static_cast<uint32_t>(cc) * (32 * BPT) + lane;
+    const T* xrow = x + static_cast<int64_t>(row) * K;
     uint4 raw[BPT][NW];
 #pragma unroll
     for (int u = 0; u < BPT; ++u) {
       const uint32_t bi = b0 + 32 * u;
-      const uint4* src = reinterpret_cast<const uint4*>(x + (row * bpr + (bi < bpr ? bi : 0)) * 16);
+      const uint4* src = reinterpret_cast<const uint4*>(xrow + static_cast<int64_t>(bi < bpr ? bi : 0) * 16);
 #pragma unroll
       for (int i = 0; i < NW; ++i) raw[u][i] = __ldg(src + i);
     }
+    const int64_t srow = LAYOUT == NVFP4_SCALES_MMA
+                             ? (static_cast<int64_t>(row >> 7) * tiles_per_row) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4
+                             : static_cast<int64_t>(row) * bpr;
 #pragma unroll
     for (int u = 0; u < BPT; ++u) {
       const uint32_t bi = b0 + 32 * u;
       if (bi >= bpr) continue;
-      const int64_t blk = row * bpr + bi;
       float v[16];
       unpack16<T>(raw[u], v);
       float ab = 0.f;
 #pragma unroll
       for (int e = 0; e < 16; ++e) ab = fmaxf(ab, fabsf(v[e]));
       const uint32_t sc = f32_to_e4m3(__fdiv_rn(ab, d));
-      uint2 packed = make_uint2(0u, 0u);
-      if (sc != 0) {
-        const float den = __fmul_rn(e4m3_to_f32(sc), st);
-        const float r = __frcp_rn(den);
-        const bool fast = den > 1e-30f && den < 1e30f;
-        packed.x = e2m1x8(v, den, r, fast);
-        packed.y = e2m1x8(v + 8, den, r, fast);
-      }
-      reinterpret_cast<uint2*>(codes)[blk] = packed;
-      const int64_t off = LAYOUT == NVFP4_SCALES_MMA ? mma_scale_offset(row, bi, cols4) : blk;
-      scales[off] = static_cast<uint8_t>(sc);
+      const uint2 packed = sc != 0 ? e2m1x16(v, __fmul_rn(e4m3_to_f32(sc), st)) : make_uint2(0u, 0u);
+      reinterpret_cast<uint2*>(codes)[static_cast<int64_t>(row) * bpr + bi] = packed;
+      scales[LAYOUT == NVFP4_SCALES_MMA ? srow + (bi >> 2) * 512 + (bi & 3) : srow + bi] = static_cast<uint8_t>(sc);
+    }
+    cc -= dcc;
+    row -= drow;
+    if (cc < 0) {
+      cc += cpr;
+      row -= 1;
     }
   }
 }

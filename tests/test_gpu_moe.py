@@ -91,3 +91,65 @@ def test_moe_config_t256_sampled_tokens():
                         [r13.get(e, r13[used[0]]) for e in range(128)],
                         [r2.get(e, r2[used[0]]) for e in range(128)])
     assert O.rel_fro(out[toks], ref) <= TOL
+
+
+# With at least 64 routed rows per expert on average the expert GEMMs run on
+# the tensor cores (tiles of up to 256 routed rows of one expert).
+@pytest.mark.parametrize("T,E,H,I,k", [(512, 8, 256, 128, 2), (300, 4, 128, 128, 1), (1024, 4, 256, 256, 2),
+                                       (700, 16, 384, 256, 3)])
+def test_tensor_core_layers(T, E, H, I, k):
+    logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=T + 1)
+    out, ids, wts = run_gpu(logits, x, w13, w2, k)
+    ref = O.moe_forward(x.float().numpy(), ids.cpu().numpy(), wts.cpu().numpy().astype(np.float64),
+                        [O.quantize(t.numpy()) for t in w13], [O.quantize(t.numpy()) for t in w2])
+    assert O.rel_fro(out, ref) <= TOL
+
+
+def test_tensor_core_skewed_routing_ragged_tiles():
+    """600 rows on one expert: tiles of 256, 256 and 88 rows; the other experts get none."""
+    T, E, H, I = 600, 4, 256, 128
+    logits, x, w13, w2 = moe_case(T, E, H, I, 1, seed=11)
+    ids = torch.full((T, 1), 1, dtype=torch.int32, device=DEV)
+    wts = torch.full((T, 1), 0.5, device=DEV)
+    out, _, _ = run_gpu(logits, x, w13, w2, 1, ids, wts)
+    ref = O.moe_forward(x.float().numpy(), np.full((T, 1), 1), np.full((T, 1), 0.5),
+                        [O.quantize(t.numpy()) for t in w13], [O.quantize(t.numpy()) for t in w2])
+    assert O.rel_fro(out, ref) <= TOL
+
+
+def test_tensor_core_deterministic_and_scaled_tokens():
+    """Repeatable bit for bit; tokens whose magnitudes span 2^-20..2^20 (the
+    per-row power-of-two shift of the f16 copies)."""
+    T, E, H, I, k = 512, 4, 128, 128, 2
+    logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=13)
+    scale = torch.pow(2.0, torch.linspace(-20, 20, T)).unsqueeze(1)
+    x = (x.float() * scale).to(torch.bfloat16)
+    a, ids, wts = run_gpu(logits, x, w13, w2, k)
+    b, _, _ = run_gpu(logits, x, w13, w2, k, ids, wts)
+    assert np.array_equal(a, b)
+    ref = O.moe_forward(x.float().numpy(), ids.cpu().numpy(), wts.cpu().numpy().astype(np.float64),
+                        [O.quantize(t.numpy()) for t in w13], [O.quantize(t.numpy()) for t in w2])
+    # per-token relative error: the rows span 40 binades
+    for t in range(0, T, 37):
+        assert O.rel_fro(a[t], ref[t]) <= TOL
+
+
+def test_moe_config_t4096_sampled_tokens():
+    """The 35B-A3B-shaped layer at T=4096 (256 routed rows per expert on
+    average: the tensor-core path), 32 sampled tokens against the oracle."""
+    m = nv()
+    T = 4096
+    logits, x, w13, w2 = synth.moe_inputs(T)
+    ids, wts = m.moe_route(logits.to(DEV), 8)
+    q13 = m.quantize_stack([w13[e].to(DEV) for e in range(128)])
+    q2 = m.quantize_stack([w2[e].to(DEV) for e in range(128)])
+    out = np_f64(m.grouped_gemm(x.to(DEV), ids, wts, q13, q2))
+    oids, ow = O.moe_route(logits.numpy(), 8)
+    toks = np.sort(np.random.default_rng(2).choice(T, 32, replace=False))
+    used = sorted(set(oids[toks].ravel().tolist()))
+    r13 = {e: O.quantize(w13[e].numpy()) for e in used}
+    r2 = {e: O.quantize(w2[e].numpy()) for e in used}
+    ref = O.moe_forward(x.float().numpy()[toks], oids[toks], ow[toks],
+                        [r13.get(e, r13[used[0]]) for e in range(128)],
+                        [r2.get(e, r2[used[0]]) for e in range(128)])
+    assert O.rel_fro(out[toks], ref) <= TOL
