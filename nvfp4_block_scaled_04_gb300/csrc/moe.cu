@@ -123,63 +123,113 @@ constexpr int PLAN_MAX_E = 4096;
 constexpr int XT_MIN_ROWS_PER_EXPERT = 64;
 
 // The whole routing plan in one CTA: count the routed rows per expert (shared
-// atomics), pad each expert to a multiple of 32 rows and prefix-sum (thread
-// 0, in expert order, also writing the tensor-core tile table: each expert's
-// rows in tiles of up to XT_NMAX), write the chunk table and row_of = -1,
-// then hand out each routed row's position within its expert (shared atomics
-// again). Replaces a memset and three kernels (count, plan, scatter).
-__global__ void __launch_bounds__(1024) route_plan_kernel(const int32_t* ids, int64_t R, int topk, int E, int* poff,
-                                                          int* chunk_count, int* chunk_expert, int* chunk_rows,
-                                                          int* tile_count, int* tile_expert, int* tile_row0,
-                                                          int* tile_rows, int* row_of, int* pos_of) {
+// atomics, four id loads in flight per thread), pad each expert to a multiple
+// of 32 rows and take the exclusive prefix sums of the padded rows and of the
+// tensor-core tiles (each expert's rows in tiles of up to XT_NMAX) with a
+// block scan, write the chunk and tile tables and row_of = -1, then hand out
+// each routed row's position within its expert (shared atomics again).
+// Replaces a memset and three kernels (count, plan, scatter).
+constexpr int PLAN_THREADS = 1024;
+__global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t* ids, int64_t R, int topk, int E,
+                                                                  int* poff, int* chunk_count, int* chunk_expert,
+                                                                  int* chunk_rows, int* tile_count, int* tile_expert,
+                                                                  int* tile_row0, int* tile_rows, int* row_of,
+                                                                  int* pos_of) {
   __shared__ int s_cnt[PLAN_MAX_E];
   __shared__ int s_off[PLAN_MAX_E];
+  __shared__ int s_wr[PLAN_THREADS / 32], s_wt[PLAN_THREADS / 32];
   __shared__ int s_total;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  for (int e = tid; e < E; e += PLAN_THREADS) s_cnt[e] = 0;
   __syncthreads();
-  for (int64_t i = threadIdx.x; i < R; i += blockDim.x) {
-    const int e = ids[i];
-    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+  for (int64_t i0 = tid; i0 < R; i0 += 4 * PLAN_THREADS) {
+    int ev[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * PLAN_THREADS;
+      ev[u] = i < R ? ids[i] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (ev[u] >= 0 && ev[u] < E) atomicAdd(&s_cnt[ev[u]], 1);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0, tiles = 0;
-    for (int e = 0; e < E; ++e) {
+  // block scan: thread tid owns experts [tid * ept, tid * ept + ept)
+  const int ept = (E + PLAN_THREADS - 1) / PLAN_THREADS;
+  int lr = 0, lt = 0;
+  for (int j = 0; j < ept; ++j) {
+    const int e = tid * ept + j;
+    if (e < E) {
+      lr += (s_cnt[e] + GV_MCHUNK - 1) / GV_MCHUNK * GV_MCHUNK;
+      lt += (s_cnt[e] + XT_NMAX - 1) / XT_NMAX;
+    }
+  }
+  int ir = lr, it = lt;   // inclusive within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, ir, o), b = __shfl_up_sync(0xffffffffu, it, o);
+    if (lane >= o) ir += a, it += b;
+  }
+  if (lane == 31) s_wr[wid] = ir, s_wt[wid] = it;
+  __syncthreads();
+  if (wid == 0) {
+    int wr = s_wr[lane], wt = s_wt[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, wr, o), b = __shfl_up_sync(0xffffffffu, wt, o);
+      if (lane >= o) wr += a, wt += b;
+    }
+    s_wr[lane] = wr, s_wt[lane] = wt;   // inclusive over warps
+  }
+  __syncthreads();
+  int acc = (wid > 0 ? s_wr[wid - 1] : 0) + ir - lr;
+  int tiles = (wid > 0 ? s_wt[wid - 1] : 0) + it - lt;
+  for (int j = 0; j < ept; ++j) {
+    const int e = tid * ept + j;
+    if (e < E) {
+      const int n = s_cnt[e];
       s_off[e] = acc;
-      for (int r = 0; r < s_cnt[e]; r += XT_NMAX, ++tiles) {
+      poff[e] = acc;
+      for (int r = 0; r < n; r += XT_NMAX, ++tiles) {
         tile_expert[tiles] = e;
         tile_row0[tiles] = acc + r;
-        tile_rows[tiles] = min(XT_NMAX, s_cnt[e] - r);
+        tile_rows[tiles] = min(XT_NMAX, n - r);
       }
-      acc += (s_cnt[e] + GV_MCHUNK - 1) / GV_MCHUNK * GV_MCHUNK;
+      for (int c = 0; c * GV_MCHUNK < n; ++c) {
+        chunk_expert[acc / GV_MCHUNK + c] = e;
+        chunk_rows[acc / GV_MCHUNK + c] = min(GV_MCHUNK, n - c * GV_MCHUNK);
+      }
+      acc += (n + GV_MCHUNK - 1) / GV_MCHUNK * GV_MCHUNK;
     }
+  }
+  if (tid == PLAN_THREADS - 1) {
     s_total = acc;
     *chunk_count = acc / GV_MCHUNK;
     *tile_count = tiles;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    poff[e] = s_off[e];
-    const int n = s_cnt[e];
-    const int c0 = s_off[e] / GV_MCHUNK;
-    for (int c = 0; c * GV_MCHUNK < n; ++c) {
-      chunk_expert[c0 + c] = e;
-      chunk_rows[c0 + c] = min(GV_MCHUNK, n - c * GV_MCHUNK);
-    }
-  }
-  for (int r = threadIdx.x; r < s_total; r += blockDim.x) row_of[r] = -1;
+  for (int r = tid; r < s_total; r += PLAN_THREADS) row_of[r] = -1;
+  for (int e = tid; e < E; e += PLAN_THREADS) s_cnt[e] = 0;
   __syncthreads();   // row_of = -1 before any position is written; counts reused as cursors
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
-  __syncthreads();
-  for (int64_t i = threadIdx.x; i < R; i += blockDim.x) {
-    const int e = ids[i];
-    if (e < 0 || e >= E) {
-      pos_of[i] = -1;
-      continue;
+  for (int64_t i0 = tid; i0 < R; i0 += 4 * PLAN_THREADS) {
+    int ev[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * PLAN_THREADS;
+      ev[u] = i < R ? ids[i] : -2;
     }
-    const int pos = s_off[e] + atomicAdd(&s_cnt[e], 1);
-    row_of[pos] = static_cast<int>(i / topk);
-    pos_of[i] = pos;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * PLAN_THREADS;
+      if (ev[u] == -2) continue;
+      if (ev[u] < 0 || ev[u] >= E) {
+        pos_of[i] = -1;
+        continue;
+      }
+      const int pos = s_off[ev[u]] + atomicAdd(&s_cnt[ev[u]], 1);
+      row_of[pos] = static_cast<int>(i / topk);
+      pos_of[i] = pos;
+    }
   }
 }
 
@@ -196,15 +246,15 @@ __global__ void __launch_bounds__(GV_THREADS) xprep_moe_row_kernel(const uint16_
 }
 
 // One warp per padded row: gather (tokens) or pass through (h), to
-// fragments. The warp reads its row once into registers (K <= 4096), takes
-// the amax with shuffles and converts (the same per-row shift and rounding as
-// xprep_row).
+// fragments. The warp reads its row once into registers (CH 16-byte pieces
+// per lane, K <= 256 * CH <= 4096), takes the amax with shuffles and converts
+// (the same per-row shift and rounding as xprep_row).
 constexpr int MOE_PREP_WARPS = 8;
 constexpr int MOE_PREP_MAX_K = 4096;
+template <int CH>
 __global__ void __launch_bounds__(MOE_PREP_WARPS * 32) xprep_moe_kernel(const uint16_t* src, int64_t K, bool gather,
                                                                          const int* row_of, const int* chunk_count,
                                                                          uint4* xfrag, int* pexp) {
-  constexpr int CH = MOE_PREP_MAX_K / 8 / 32;   // 16-byte chunks per lane
   const int64_t r = static_cast<int64_t>(blockIdx.x) * MOE_PREP_WARPS + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= static_cast<int64_t>(*chunk_count) * GV_MCHUNK) return;
@@ -253,12 +303,13 @@ __global__ void __launch_bounds__(MOE_PREP_WARPS * 32) xprep_moe_kernel(const ui
 }
 
 // The same per-row conversion into row-major f16 rows [padded rows][K] (the
-// tensor-core path's B operand, read by TMA): one warp per padded row.
+// tensor-core path's B operand, read by TMA): one warp per padded row, CH
+// 16-byte pieces per lane (K <= 256 * CH), so short rows keep few registers.
+template <int CH>
 __global__ void __launch_bounds__(MOE_PREP_WARPS * 32) xprep_moe_rows_kernel(const uint16_t* src, int64_t K,
                                                                               bool gather, const int* row_of,
                                                                               const int* chunk_count, uint4* xrow,
                                                                               int* pexp) {
-  constexpr int CH = MOE_PREP_MAX_K / 8 / 32;   // 16-byte chunks per lane
   const int64_t r = static_cast<int64_t>(blockIdx.x) * MOE_PREP_WARPS + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= static_cast<int64_t>(*chunk_count) * GV_MCHUNK) return;
@@ -346,9 +397,13 @@ int launch_moe_tma(const nvfp4_tensor_t& W, int box_rows, const TmaSkinnyParams&
 int prep_moe(const uint16_t* src, int64_t K, bool gather, const MoeWs& m, uint4* xfrag, int* pexp,
              cudaStream_t stream) {
   const int64_t prow = m.max_chunks * GV_MCHUNK;
-  if (K <= MOE_PREP_MAX_K)
-    xprep_moe_kernel<<<static_cast<unsigned>(ceil_div(prow, MOE_PREP_WARPS)), MOE_PREP_WARPS * 32, 0, stream>>>(
-        src, K, gather, m.row_of, m.chunk_count, xfrag, pexp);
+  const dim3 grid(static_cast<unsigned>(ceil_div(prow, MOE_PREP_WARPS))), block(MOE_PREP_WARPS * 32);
+  if (K <= 1024)
+    xprep_moe_kernel<4><<<grid, block, 0, stream>>>(src, K, gather, m.row_of, m.chunk_count, xfrag, pexp);
+  else if (K <= 2048)
+    xprep_moe_kernel<8><<<grid, block, 0, stream>>>(src, K, gather, m.row_of, m.chunk_count, xfrag, pexp);
+  else if (K <= MOE_PREP_MAX_K)
+    xprep_moe_kernel<16><<<grid, block, 0, stream>>>(src, K, gather, m.row_of, m.chunk_count, xfrag, pexp);
   else
     xprep_moe_row_kernel<<<static_cast<unsigned>(prow), GV_THREADS, 0, stream>>>(src, K, gather, m.row_of,
                                                                                   m.chunk_count, xfrag, pexp);
@@ -359,8 +414,14 @@ int prep_moe(const uint16_t* src, int64_t K, bool gather, const MoeWs& m, uint4*
 int prep_moe_rows(const uint16_t* src, int64_t K, bool gather, const MoeWs& m, void* xrow, int* pexp,
                   cudaStream_t stream) {
   const int64_t prow = m.max_chunks * GV_MCHUNK;
-  xprep_moe_rows_kernel<<<static_cast<unsigned>(ceil_div(prow, MOE_PREP_WARPS)), MOE_PREP_WARPS * 32, 0, stream>>>(
-      src, K, gather, m.row_of, m.chunk_count, static_cast<uint4*>(xrow), pexp);
+  const dim3 grid(static_cast<unsigned>(ceil_div(prow, MOE_PREP_WARPS))), block(MOE_PREP_WARPS * 32);
+  uint4* dst = static_cast<uint4*>(xrow);
+  if (K <= 1024)
+    xprep_moe_rows_kernel<4><<<grid, block, 0, stream>>>(src, K, gather, m.row_of, m.chunk_count, dst, pexp);
+  else if (K <= 2048)
+    xprep_moe_rows_kernel<8><<<grid, block, 0, stream>>>(src, K, gather, m.row_of, m.chunk_count, dst, pexp);
+  else
+    xprep_moe_rows_kernel<16><<<grid, block, 0, stream>>>(src, K, gather, m.row_of, m.chunk_count, dst, pexp);
   return from_cuda(cudaGetLastError());
 }
 
@@ -414,7 +475,7 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
   const int64_t R = T * topk;
   if (E > PLAN_MAX_E) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   const MoeWs m = carve_moe(ws, T, H, I, E, topk);
-  route_plan_kernel<<<1, 1024, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.chunk_count,
+  route_plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.chunk_count,
                                             m.chunk_expert, m.chunk_rows, m.tile_count, m.tile_expert, m.tile_row0,
                                             m.tile_rows, m.row_of, m.pos_of);
   int rc = from_cuda(cudaGetLastError());

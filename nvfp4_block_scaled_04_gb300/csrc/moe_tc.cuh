@@ -33,13 +33,16 @@ namespace nvfp4 {
 namespace {
 
 constexpr int XT_BK = 64;                                // K per stage
-constexpr int XT_STAGES = 6;
-constexpr int XT_NMAX = 256;                             // routed rows per tile
+constexpr int XT_NMAX = 128;                             // routed rows per tile
+// two CTAs per SM with 128-row tiles (one's prologue and epilogue run beside
+// the other's main loop), one with 256-row tiles
+constexpr int XT_CTAS_PER_SM = XT_NMAX == 256 ? 1 : 2;
+constexpr int XT_STAGES = XT_NMAX == 256 ? 6 : 4;
 constexpr int XT_B_BYTES = XT_NMAX * 128;                // rows x 64 f16
 constexpr int XT_C_BYTES = 128 * 32;                     // 128 weight rows x 32 code bytes
-constexpr int XT_STAGE_BYTES = XT_B_BYTES + XT_C_BYTES;  // 36 KB, a multiple of 1024
-constexpr int XT_A_COL0 = 256;                           // tensor memory: accumulator [0, 256), A slots after
-constexpr int XT_TMEM_COLS = 512;
+constexpr int XT_STAGE_BYTES = XT_B_BYTES + XT_C_BYTES;  // a multiple of 1024
+constexpr int XT_A_COL0 = XT_NMAX;                       // tensor memory: accumulator [0, NMAX), A slots after
+constexpr int XT_TMEM_COLS = XT_NMAX == 256 ? 512 : 256;
 constexpr int XT_DQ_WARPS = 8;
 constexpr int XT_THREADS = (2 + XT_DQ_WARPS) * 32;
 constexpr int XT_EPI_THREADS = XT_DQ_WARPS * 32;
@@ -47,7 +50,7 @@ constexpr int XT_BARS = 3 * XT_STAGES + 1;
 constexpr int XT_SMEM = XT_STAGES * XT_STAGE_BYTES + 1024 /*alignment*/ + 256 /*barriers, slot, flag*/;
 static_assert(XT_A_COL0 + XT_STAGES * 32 <= XT_TMEM_COLS, "tensor memory columns");
 static_assert(XT_BARS * 8 + 16 <= 256, "barrier area");
-static_assert((2 * 64 * 33 + XT_NMAX) * 4 <= XT_B_BYTES, "epilogue buffers fit in a stage");
+static_assert((2 * 64 * 33 + XT_NMAX) * 4 <= XT_STAGES * XT_STAGE_BYTES, "epilogue buffers fit in the ring");
 
 struct MoeTcParams {
   const uint8_t* scales;   // row-major block scales of the stacked weights [E * rows_per_expert][K / 16]
@@ -93,7 +96,7 @@ NVFP4_DEV bool xt_all_epilogue(bool pred) {
 NVFP4_DEV void xt_epilogue_sync() { asm volatile("bar.sync 1, %0;" ::"n"(XT_EPI_THREADS) : "memory"); }
 
 template <bool GATEUP>
-__global__ void __launch_bounds__(XT_THREADS, 1)
+__global__ void __launch_bounds__(XT_THREADS, XT_CTAS_PER_SM)
     moe_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                   const MoeTcParams p) {
   const int tile = static_cast<int>(blockIdx.y);
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
     const bool acc_ok = __all_sync(0xffffffffu, mbar_wait_bounded(accf_bar, 0, abort_flag, p.status));
     tc_fence_after();
     if (xt_all_epilogue(ok && acc_ok && *abort_flag == 0)) {
-      // stage 0 is free once the MMAs completed: gate and up values of 32
+      // the ring is free once the MMAs completed: gate and up values of 32
       // routed rows ([64][33] each, padded against bank conflicts), then the
       // per-row output multipliers s_t * 2^shift
       float* gbuf = reinterpret_cast<float*>(base_ptr);
