@@ -483,7 +483,7 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
 
   // Many rows per expert: the tensor cores (the f16 rows live where the
   // fragment-order copies would).
-  if (R >= XT_MIN_ROWS_PER_EXPERT * E && m.max_tiles <= 65535 && H % 128 == 0 && I % 128 == 0 && H <= MOE_PREP_MAX_K &&
+  if (R >= XT_MIN_ROWS_PER_EXPERT * E && m.max_tiles <= 65535 && H % 256 == 0 && I % 256 == 0 && H <= MOE_PREP_MAX_K &&
       I <= MOE_PREP_MAX_K && ((reinterpret_cast<uintptr_t>(W13.scales) | reinterpret_cast<uintptr_t>(W2.scales)) & 3) == 0) {
     rc = prep_moe_rows(X, H, true, m, m.xfrag1, m.pexp1, stream);
     if (rc != NVFP4_OK) return rc;

@@ -60,7 +60,7 @@ struct MoeTcParams {
   const int* tile_expert;
   const int* tile_row0;
   const int* tile_rows;
-  int K;
+  int K;                   // a multiple of 256
   int rows_per_expert;     // gate/up: 2I, down: H
   int inter;               // I
   int hidden;              // H
@@ -193,23 +193,25 @@ __global__ void __launch_bounds__(XT_THREADS, XT_CTAS_PER_SM)
     const int half = dw >> 2;             // which 32 K of each stage
     const int r = quarter * 32 + lane;    // tensor-memory lane = weight row of the tile
     const int64_t grow = GATEUP ? (r < 64 ? wrow0 + r : wrow0 + p.inter + (r - 64)) : wrow0 + r;
-    const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + grow * (p.K / 16));
     const uint32_t a_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + XT_A_COL0 + 16 * half;
-    // block scales of stages ks .. ks + 3 in flight (4 bytes = four 16-K blocks per stage)
-    uint32_t sc0 = 0 < n_k ? __ldg(srow + 0) : 0u, sc1 = 1 < n_k ? __ldg(srow + 1) : 0u;
-    uint32_t sc2 = 2 < n_k ? __ldg(srow + 2) : 0u, sc3 = 3 < n_k ? __ldg(srow + 3) : 0u;
+    // block scales: 16 bytes of a row cover four stages (K % 256 == 0), word j
+    // the four 16-K blocks of stage j; group g + 1 is requested while group g
+    // is in use
+    const uint4* sgrp = reinterpret_cast<const uint4*>(p.scales + grow * (p.K / 16));
+    const int n_grp = n_k / 4;
+    uint4 sc_cur = __ldg(sgrp), sc_next = n_grp > 1 ? __ldg(sgrp + 1) : make_uint4(0u, 0u, 0u, 0u);
     bool ok = true;
     for (int ks = 0; ks < n_k; ++ks) {
       const int s = ks % XT_STAGES;
+      if ((ks & 3) == 0 && ks > 0) {
+        sc_cur = sc_next;
+        if ((ks >> 2) + 1 < n_grp) sc_next = __ldg(sgrp + (ks >> 2) + 1);
+      }
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(full_bar(s), (ks / XT_STAGES) & 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
-      const uint32_t sc = sc0;
-      sc0 = sc1;
-      sc1 = sc2;
-      sc2 = sc3;
-      sc3 = ks + 4 < n_k ? __ldg(srow + ks + 4) : 0u;
+      const uint32_t sc = (ks & 3) == 0 ? sc_cur.x : (ks & 3) == 1 ? sc_cur.y : (ks & 3) == 2 ? sc_cur.z : sc_cur.w;
       const uint32_t s01 = e4m3x2_to_f16x2(half ? (sc >> 16) : (sc & 0xFFFFu));
       const uint32_t bscale[2] = {dup_lo(s01), dup_hi(s01)};
       const uint4 c = lds128(stage_c(s) + r * 32 + 16 * half);

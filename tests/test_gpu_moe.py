@@ -93,10 +93,11 @@ def test_moe_config_t256_sampled_tokens():
     assert O.rel_fro(out[toks], ref) <= TOL
 
 
-# With at least 64 routed rows per expert on average the expert GEMMs run on
-# the tensor cores (tiles of up to 256 routed rows of one expert).
-@pytest.mark.parametrize("T,E,H,I,k", [(512, 8, 256, 128, 2), (300, 4, 128, 128, 1), (1024, 4, 256, 256, 2),
-                                       (700, 16, 384, 256, 3)])
+# With at least 64 routed rows per expert on average (and H, I multiples of
+# 256) the expert GEMMs run on the tensor cores: tiles of up to 128 routed
+# rows of one expert.
+@pytest.mark.parametrize("T,E,H,I,k", [(512, 8, 256, 256, 2), (300, 4, 256, 256, 1), (1024, 4, 256, 512, 2),
+                                       (700, 16, 512, 256, 3)])
 def test_tensor_core_layers(T, E, H, I, k):
     logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=T + 1)
     out, ids, wts = run_gpu(logits, x, w13, w2, k)
@@ -106,8 +107,8 @@ def test_tensor_core_layers(T, E, H, I, k):
 
 
 def test_tensor_core_skewed_routing_ragged_tiles():
-    """600 rows on one expert: tiles of 256, 256 and 88 rows; the other experts get none."""
-    T, E, H, I = 600, 4, 256, 128
+    """600 rows on one expert: four tiles of 128 rows and one of 88; the other experts get none."""
+    T, E, H, I = 600, 4, 256, 256
     logits, x, w13, w2 = moe_case(T, E, H, I, 1, seed=11)
     ids = torch.full((T, 1), 1, dtype=torch.int32, device=DEV)
     wts = torch.full((T, 1), 0.5, device=DEV)
@@ -120,7 +121,7 @@ def test_tensor_core_skewed_routing_ragged_tiles():
 def test_tensor_core_deterministic_and_scaled_tokens():
     """Repeatable bit for bit; tokens whose magnitudes span 2^-20..2^20 (the
     per-row power-of-two shift of the f16 copies)."""
-    T, E, H, I, k = 512, 4, 128, 128, 2
+    T, E, H, I, k = 512, 4, 256, 256, 2
     logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=13)
     scale = torch.pow(2.0, torch.linspace(-20, 20, T)).unsqueeze(1)
     x = (x.float() * scale).to(torch.bfloat16)
