@@ -119,8 +119,11 @@ MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
 }
 
 constexpr int PLAN_MAX_E = 4096;
-// average routed rows per expert from which the expert GEMMs run on the tensor cores
-constexpr int XT_MIN_ROWS_PER_EXPERT = 64;
+// average routed rows per expert from which the expert GEMMs run on the tensor
+// cores (128 experts, top-8, H = 2048, I = 768: 16 rows per expert 0.158 ms
+// on the skinny kernel against 0.169 on the tensor cores, 32 rows 0.226
+// against 0.183)
+constexpr int XT_MIN_ROWS_PER_EXPERT = 32;
 
 // The whole routing plan in one CTA: count the routed rows per expert (shared
 // atomics, four id loads in flight per thread), pad each expert to a multiple

@@ -93,11 +93,11 @@ def test_moe_config_t256_sampled_tokens():
     assert O.rel_fro(out[toks], ref) <= TOL
 
 
-# With at least 64 routed rows per expert on average (and H, I multiples of
+# With at least 32 routed rows per expert on average (and H, I multiples of
 # 256) the expert GEMMs run on the tensor cores: tiles of up to 128 routed
 # rows of one expert.
 @pytest.mark.parametrize("T,E,H,I,k", [(512, 8, 256, 256, 2), (300, 4, 256, 256, 1), (1024, 4, 256, 512, 2),
-                                       (700, 16, 512, 256, 3)])
+                                       (700, 16, 512, 256, 3), (128, 8, 256, 256, 2)])
 def test_tensor_core_layers(T, E, H, I, k):
     logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=T + 1)
     out, ids, wts = run_gpu(logits, x, w13, w2, k)
