@@ -187,8 +187,8 @@ int nvfp4_moe_route(const float* logits, int64_t T, int E, int topk,
  * least 32 routed rows on average (T * topk >= 32 E), with H and I multiples
  * of 256, run the expert GEMMs on the tensor cores; others on the streaming
  * kernel. Both compute the products exactly and sum in fp32 (the summation
- * order differs between them). On either path a routed row's result does not
- * depend on the other rows, and repeated calls give identical outputs. */
+ * order differs between them). Repeated calls with the same inputs give
+ * identical outputs. */
 int nvfp4_grouped_gemm(const void* X, int64_t T, int topk, const int32_t* topk_ids,
                        const float* topk_w, nvfp4_tensor_t W13, nvfp4_tensor_t W2,
                        void* out, void* workspace, size_t workspace_bytes,
