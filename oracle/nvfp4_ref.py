@@ -44,6 +44,11 @@ Readings where the pages are silent (each is listed in the design doc):
      W13 rows [0, I) are the gate, [I, 2I) the up projection;
      h = bf16(silu(g) * u); out = sum_j w_j * (h_j @ W2_e^T).
      Each expert matrix carries its own tensor scale.
+  R10 W4A4 MoE     (the routed experts with 4-bit activations as well): the
+     layer input is quantised once per call with its own dynamic tensor scale
+     and each routed row is its token's quantised row; h as in R7; the h rows
+     of all routed (token, slot) pairs are quantised together, one dynamic
+     tensor scale per call, before the down projection.
 
 The quantiser takes its decisions in fp32 (numpy float32 arithmetic is IEEE
 round-to-nearest-even with no fused multiply-add), the precision the GPU
@@ -310,4 +315,34 @@ def moe_forward(x, ids, weights, w13: list, w2: list):
         h = bf16_round(silu(gu[:, :inter]) * gu[:, inter:])
         y = h @ decode(w2[e]).T
         np.add.at(out, tok, weights[tok, slot][:, None] * y)
+    return out
+
+
+def moe_forward_w4a4(x, ids, weights, w13: list, w2: list):
+    """R10: the R7 layer with NVFP4 activations into both expert projections
+    (What 350+ Experiments..., section 7: the NVFP4 mixture-of-experts
+    kernels). x_hat = decode(quantise(x)) with one dynamic tensor scale for the
+    call; [g; u] = x_hat[t] @ W13_e^T; h = bf16(silu(g) * u) for every routed
+    (t, j); h_hat = decode(quantise(all routed h rows)), one dynamic tensor
+    scale for the call; out[t] = sum_j w[t,j] * (h_hat[t,j] @ W2_e^T).
+    Decoded products summed in fp64 (R5)."""
+    x = np.asarray(x, dtype=np.float32)
+    ids = np.asarray(ids)
+    weights = np.asarray(weights, dtype=np.float64)
+    T = x.shape[0]
+    xd = decode(quantize(x))
+    tok, slot = np.nonzero((ids >= 0) & (ids < len(w13)))
+    exp = ids[tok, slot]
+    inter = w13[0].shape[0] // 2
+    h = np.zeros((tok.size, inter), dtype=np.float64)
+    for e in np.unique(exp):
+        r = np.nonzero(exp == e)[0]
+        gu = xd[tok[r]] @ decode(w13[e]).T
+        h[r] = bf16_round(silu(gu[:, :inter]) * gu[:, inter:])
+    hd = decode(quantize(h.astype(np.float32))) if tok.size else h   # bf16 values are exact in fp32
+    out = np.zeros((T, w2[0].shape[0]), dtype=np.float64)
+    for e in np.unique(exp):
+        r = np.nonzero(exp == e)[0]
+        y = hd[r] @ decode(w2[e]).T
+        np.add.at(out, tok[r], weights[tok[r], slot[r]][:, None] * y)
     return out

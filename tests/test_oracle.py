@@ -411,3 +411,74 @@ def test_moe_is_linear_in_routing_weights_and_permutes_with_tokens():
     perm = rng.permutation(T)
     outp = O.moe_forward(x[perm], ids[perm], w[perm], w13, w2)
     np.testing.assert_allclose(outp, out[perm], rtol=1e-13, atol=1e-15)
+
+
+# --- R10, W4A4 routed experts ------------------------------------------------
+
+def _moe4_case(seed=21):
+    rng, x, w13, w2 = _small_moe(seed=seed)
+    T = x.shape[0]
+    ids, w = O.moe_route(rng.standard_normal((T, 4)), 2)
+    return rng, x, w13, w2, ids, w
+
+
+def test_moe_w4a4_sees_only_the_quantised_input():
+    """Nudging input elements without changing their codes, block scales or
+    the tensor scale leaves the layer bit-identical (while the W4A16 layer
+    moves), so the input enters only through its quantised form."""
+    rng, x, w13, w2, ids, w = _moe4_case()
+    q0 = O.quantize(x)
+    blocks = np.abs(x).reshape(x.shape[0], -1, 16)
+    is_max = (blocks == blocks.max(axis=2, keepdims=True)).reshape(x.shape)
+    xn = np.where(is_max, x, x * np.float32(1 + 2.0 ** -14)).astype(np.float32)
+    qn = O.quantize(xn)
+    # keep only the nudges that leave every code of their block unchanged
+    same = (O.unpack_codes(qn.codes) == O.unpack_codes(q0.codes)).reshape(x.shape[0], -1, 16).all(axis=2)
+    xn = np.where(np.repeat(same, 16, axis=1), xn, x).astype(np.float32)
+    qn = O.quantize(xn)
+    assert np.array_equal(qn.codes, q0.codes) and np.array_equal(qn.scales, q0.scales) and qn.s_t == q0.s_t
+    assert not np.array_equal(xn, x)
+    a = O.moe_forward_w4a4(x, ids, w, w13, w2)
+    b = O.moe_forward_w4a4(xn, ids, w, w13, w2)
+    assert np.array_equal(a, b)
+    assert not np.array_equal(O.moe_forward(x, ids, w, w13, w2), O.moe_forward(xn, ids, w, w13, w2))
+
+
+def test_moe_w4a4_is_near_the_w4a16_layer_on_the_quantised_input():
+    """Against the R7 layer fed the decoded quantised input, only the h
+    quantisation differs: a small, non-zero change."""
+    rng, x, w13, w2, ids, w = _moe4_case()
+    a = O.moe_forward_w4a4(x, ids, w, w13, w2)
+    b = O.moe_forward(O.decode(O.quantize(x)), ids, w, w13, w2)
+    e = O.rel_fro(a, b)
+    assert 0 < e < 0.1
+
+
+def test_moe_w4a4_h_scale_is_shared_by_all_routed_rows():
+    """A token on another expert whose h is the largest of the call changes
+    every other token's output (one tensor scale for all h rows); a token
+    whose h stays below that maximum changes nothing."""
+    rng, x, w13, w2, ids, w = _moe4_case()
+    T = x.shape[0]
+    ids = np.where(ids == 3, 0, ids)              # the base tokens avoid expert 3
+    base = O.moe_forward_w4a4(x, ids, w, w13, w2)
+    w13_big = list(w13)
+    w13_big[3] = O.quantize((O.decode(w13[3]) * 64).astype(np.float32))
+    x_dup = np.concatenate([x, x[:1]])            # same rows: the input's tensor scale is unchanged
+    ids_new = np.concatenate([ids, [[3, 3]]])
+    w_new = np.concatenate([w, [[0.5, 0.5]]])
+    big = O.moe_forward_w4a4(x_dup, ids_new, w_new, w13_big, w2)
+    assert not np.array_equal(big[:T], base)
+    x_small = np.concatenate([x, x[:1] * np.float32(2.0 ** -6)])
+    small = O.moe_forward_w4a4(x_small, ids_new, w_new, w13, w2)
+    assert np.array_equal(small[:T], base)
+
+
+def test_moe_w4a4_permutes_with_tokens_and_scales_with_routing_weights():
+    rng, x, w13, w2, ids, w = _moe4_case()
+    T = x.shape[0]
+    out = O.moe_forward_w4a4(x, ids, w, w13, w2)
+    perm = rng.permutation(T)
+    np.testing.assert_allclose(O.moe_forward_w4a4(x[perm], ids[perm], w[perm], w13, w2), out[perm],
+                               rtol=1e-13, atol=1e-15)
+    assert np.array_equal(O.moe_forward_w4a4(x, ids, 2 * w, w13, w2), 2 * out)

@@ -67,6 +67,33 @@ def _argmax_first_position(logits, rows):
     return np.asarray(rows)[pos], logits.max(axis=1)
 
 
+def _moe_w4a4_mutant(quant_x=True, quant_h=True, per_expert_h=False, swap_gu=False):
+    """The R10 layer with one planted mistake."""
+    def f(x, ids, weights, w13, w2):
+        x = np.asarray(x, dtype=np.float32)
+        ids = np.asarray(ids)
+        weights = np.asarray(weights, dtype=np.float64)
+        xd = R.decode(R.quantize(x)) if quant_x else x.astype(np.float64)
+        tok, slot = np.nonzero(ids >= 0)
+        exp = ids[tok, slot]
+        inter = w13[0].shape[0] // 2
+        h = np.zeros((tok.size, inter))
+        for e in np.unique(exp):
+            r = np.nonzero(exp == e)[0]
+            gu = xd[tok[r]] @ R.decode(w13[e]).T
+            g, u = (gu[:, inter:], gu[:, :inter]) if swap_gu else (gu[:, :inter], gu[:, inter:])
+            h[r] = R.bf16_round(R.silu(g) * u)
+        if quant_h and not per_expert_h:
+            h = R.decode(R.quantize(h.astype(np.float32)))
+        out = np.zeros((x.shape[0], w2[0].shape[0]))
+        for e in np.unique(exp):
+            r = np.nonzero(exp == e)[0]
+            he = R.decode(R.quantize(h[r].astype(np.float32))) if per_expert_h else h[r]
+            np.add.at(out, tok[r], weights[tok[r], slot[r]][:, None] * (he @ R.decode(w2[e]).T))
+        return out
+    return f
+
+
 def _golden_all():
     for blk in P.load_blocks():
         P.test_golden_block(blk)
@@ -94,6 +121,19 @@ MUTANTS = {
     "routing renormalised": (
         lambda mp: _set(mp, "moe_route", _route_renormalised),
         [P.test_route_matches_sorting]),
+    "W4A4 MoE input not quantised": (
+        lambda mp: _set(mp, "moe_forward_w4a4", _moe_w4a4_mutant(quant_x=False)),
+        [P.test_moe_w4a4_sees_only_the_quantised_input]),
+    "W4A4 MoE h not quantised": (
+        lambda mp: _set(mp, "moe_forward_w4a4", _moe_w4a4_mutant(quant_h=False)),
+        [P.test_moe_w4a4_is_near_the_w4a16_layer_on_the_quantised_input,
+         P.test_moe_w4a4_h_scale_is_shared_by_all_routed_rows]),
+    "W4A4 MoE h scale per expert": (
+        lambda mp: _set(mp, "moe_forward_w4a4", _moe_w4a4_mutant(per_expert_h=True)),
+        [P.test_moe_w4a4_h_scale_is_shared_by_all_routed_rows]),
+    "W4A4 MoE gate and up swapped": (
+        lambda mp: _set(mp, "moe_forward_w4a4", _moe_w4a4_mutant(swap_gu=True)),
+        [P.test_moe_w4a4_is_near_the_w4a16_layer_on_the_quantised_input]),
     "argmax by first position": (
         lambda mp: _set(mp, "argmax_lowest_id", _argmax_first_position),
         [P.test_argmax_ties_go_to_lowest_vocab_id]),
