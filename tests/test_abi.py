@@ -121,3 +121,37 @@ def test_row_gather_and_compact_argmax_validate_arguments(nv):
     Wa = nv.CTensor(0x1000, 0x2000, 0x3000, 64, 384, 1, 0)
     assert L.nvfp4_gemv_argmax(_fake(), 1, Wa, None, _fake(), None, ws, 1 << 20, None) == -2  # K % 256
     assert L.nvfp4_gemv_argmax(_fake(), 1, W, None, _fake(), None, None, 0, None) == -5       # workspace
+
+
+def test_grouped_gemm_validates_arguments(nv):
+    L = nv.lib()
+    ws = _fake(0x20000)
+    E, H, I = 4, 256, 256
+    W13 = nv.CTensor(0x30000, 0x40000, 0x50000, 2 * I, H, E, 0)
+    W2 = nv.CTensor(0x60000, 0x70000, 0x80000, H, I, E, 0)
+    need = nv.workspace_size(nv.OP_GROUPED_GEMM, 64, H, I, E, 2)
+    args = (_fake(), 64, 2, _fake(), _fake())
+    assert L.nvfp4_grouped_gemm(*args, W13, W2, _fake(), ws, need - 1, None) == -5          # workspace short
+    assert L.nvfp4_grouped_gemm(*args, W13, W2, _fake(), None, 0, None) == -5               # no workspace
+    assert L.nvfp4_grouped_gemm(_fake(0x10008), 64, 2, _fake(), _fake(), W13, W2, _fake(), ws, need,
+                                None) == -3                                                  # X misaligned
+    assert L.nvfp4_grouped_gemm(_fake(), 64, 5, _fake(), _fake(), W13, W2, _fake(), ws, 1 << 30,
+                                None) == -1                                                  # topk > E
+    assert L.nvfp4_grouped_gemm(_fake(), 64, 0, _fake(), _fake(), W13, W2, _fake(), ws, 1 << 30,
+                                None) == -1                                                  # topk < 1
+    W13m = nv.CTensor(0x30000, 0x40000, 0x50000, 2 * I, H, E, 1)
+    assert L.nvfp4_grouped_gemm(*args, W13m, W2, _fake(), ws, 1 << 30, None) == -1          # MMA scales
+    W13k = nv.CTensor(0x30000, 0x40000, 0x50000, 2 * I, 192, E, 0)
+    W2k = nv.CTensor(0x60000, 0x70000, 0x80000, 192, I, E, 0)
+    assert L.nvfp4_grouped_gemm(*args, W13k, W2k, _fake(), ws, 1 << 30, None) == -2        # H % 128
+    assert L.nvfp4_grouped_gemm(_fake(), 0, 2, _fake(), _fake(), W13, W2, _fake(), None, 0, None) == 0   # T = 0
+
+
+def test_grouped_workspace_holds_the_tile_table(nv):
+    """The tensor-core tile table (up to 128 routed rows of one expert per
+    tile) grows the workspace with T and E, in steps of whole tables."""
+    H, I = 2048, 768
+    small = nv.workspace_size(nv.OP_GROUPED_GEMM, 4096, H, I, 128, 8)
+    more_experts = nv.workspace_size(nv.OP_GROUPED_GEMM, 4096, H, I, 256, 8)
+    assert more_experts > small
+    assert nv.workspace_size(nv.OP_GROUPED_GEMM, 4096 + 16, H, I, 128, 8) > small
