@@ -2,10 +2,11 @@
  * nvfp4.h - C ABI of libnvfp4.so: the NVFP4 block-scaled linear layer of a
  * 4-bit LLM serving engine, on one NVIDIA GB300 (sm_103a).
  *
- * The format. "NVFP4 is 4-bit e2m1 with per-16 FP8 scales" (Serving
- * Qwen3.8-27B in 4-bit with a masked speculative decoding head, "What the
- * artifact is"); the FP8 scale is E4M3, four exponent and three mantissa bits
- * (What 350+ Experiments Taught Us About Serving Qwen 3.6 35B-A3B, section 3).
+ * The format. Values are 4-bit e2m1 codes, and every 16 consecutive elements
+ * along K share one 8-bit floating-point block scale (Serving Qwen3.8-27B in
+ * 4-bit with a masked speculative decoding head, "What the artifact is"); that
+ * scale is E4M3, four exponent and three mantissa bits (What 350+ Experiments
+ * Taught Us About Serving Qwen 3.6 35B-A3B, section 3).
  * A tensor T[rows][K] is stored as
  *   codes   uint8 [rows][K/2]   element 2j in the low nibble of byte j,
  *                               element 2j+1 in the high nibble;
@@ -27,6 +28,11 @@
  *  - Base pointers of codes, activations and outputs must be 16-byte aligned.
  *  - No CPU fallback exists: every call runs CUDA kernels on the current
  *    device.
+ *  - Per device, the library caches device addresses of its own device
+ *    variables (the status word, the fixed scratch of the allocation-free
+ *    entry point) and kernel attributes on first use. cudaDeviceReset
+ *    invalidates them: do not use the library on a device after resetting it
+ *    in the same process.
  */
 #ifndef NVFP4_H_
 #define NVFP4_H_
@@ -120,9 +126,9 @@ int nvfp4_prepack_scales(const uint8_t* src, int64_t batch, int64_t rows, int64_
                          uint8_t* dst, nvfp4_stream_t stream);
 
 /* W4A16 linear (decode): Y[m][n] = bf16( sum_k X[m][k] * W_hat[n][k] ) with
- * fp32 accumulation - "four-bit weights and 16-bit activations" (What 350+
- * Experiments..., section 1; Qwen3.8-27B benchmark, "Serving configuration
- * measured").
+ * fp32 accumulation: 4-bit weights against 16-bit activations, the decode form
+ * of the layer (What 350+ Experiments..., section 1; Qwen3.8-27B benchmark,
+ * "Serving configuration measured").
  *   X  device bf16 [M][K];  W  NVFP4 [N][K], batch 1, ROWMAJOR scales;
  *   Y  device bf16 [M][N].
  *   workspace  >= nvfp4_workspace_size(NVFP4_OP_GEMM_W4A16, M, N, K) bytes:
@@ -139,8 +145,12 @@ int nvfp4_gemm_w4a16(const void* X, int64_t M, nvfp4_tensor_t W, void* Y,
  * their decode path - an engine that reserves nearly all device memory for its
  * KV cache at start-up, or a host that must not call cudaMalloc / cudaFree
  * there because those calls can synchronise the device.
- *   X, M, W, Y as for nvfp4_gemm_w4a16; 1 <= M <= 32, K <= 32768, else
- *   NVFP4_ERR_SCRATCH_LIMIT before anything is launched.
+ *   X, M, W, Y as for nvfp4_gemm_w4a16; 1 <= M <= 32, K <= 32768 and the
+ *   workspace nvfp4_workspace_size(NVFP4_OP_GEMM_W4A16, M, N, K) would need
+ *   at most 8 MiB (true for every such shape on a GPU of up to 152 SMs: the
+ *   split-K partials take at most 2 * SMs * 16 KiB, the converted activations
+ *   at most 2 MiB); otherwise NVFP4_ERR_SCRATCH_LIMIT before anything is
+ *   launched.
  * The first call on each device (with that device current) looks up the
  * array's device address with cudaGetSymbolAddress; make it before any
  * stream capture. All calls share the array: calls that overlap on the GPU
@@ -150,9 +160,9 @@ int nvfp4_gemm_w4a16_noalloc(const void* X, int64_t M, nvfp4_tensor_t W, void* Y
 
 /* W4A4 linear (prefill): Y[m][n] = bf16( s_tA * s_tW * sum_k a[m][k] * w[n][k] )
  * where a, w are the e2m1*e4m3 products, multiplied and accumulated (fp32) by
- * the block-scaled FP4 tensor cores - "Blackwell-native NVFP4 W4A4 execution"
- * (52.6% More Tokens, 1.53x Less GPU Time: Production Inference with Minima
- * and Rafay).
+ * the block-scaled FP4 tensor cores: both operands 4-bit, run natively on
+ * Blackwell (52.6% More Tokens, 1.53x Less GPU Time: Production Inference
+ * with Minima and Rafay, comparison paragraph).
  *   A  NVFP4 [M][K] (typically from nvfp4_quantize, COMPUTE);
  *   W  NVFP4 [N][K]; both batch 1. MMA-layout scales are used in place;
  *      ROWMAJOR scales are re-laid into the workspace first.
@@ -177,7 +187,10 @@ int nvfp4_moe_route(const float* logits, int64_t T, int E, int topk,
  *     h      = bf16( silu(g) * u )
  *     out[t] += topk_w[t][j] * (h @ W2_e^T)
  *   out = bf16(sum over j, fp32, in slot order).
- *   X        device bf16 [T][H];  topk_ids int32 [T][topk] (each in [0, E));
+ *   X        device bf16 [T][H];  topk_ids int32 [T][topk]: a slot whose id
+ *            lies outside [0, E) is dropped (it adds nothing to out[t]) and
+ *            sets NVFP4_ERR_INVALID_ARG in the device status word
+ *            (nvfp4_read_device_status);
  *   topk_w   fp32 [T][topk];
  *   W13      NVFP4, batch E, rows 2I, K H, ROWMAJOR;
  *   W2       NVFP4, batch E, rows H,  K I, ROWMAJOR;
@@ -238,6 +251,29 @@ int nvfp4_gather_rows(nvfp4_tensor_t W, const int32_t* idx, int64_t n_idx, uint8
 int nvfp4_gemv_argmax(const void* H, int64_t M, nvfp4_tensor_t W, const int32_t* ids, int32_t* out_ids,
                       float* out_logit, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
+/* Speculative verify head: the full-vocabulary GEMV + argmax of
+ * nvfp4_gemv_argmax over every row of the LM head W, with a batched greedy
+ * acceptance of the drafts fused into its last step. The draft proposes from
+ * the masked head, verification reads the whole vocabulary (Serving
+ * Qwen3.8-27B in 4-bit..., "The masked head trick"); the verify change of
+ * the Qwen3.8-27B benchmark ("Sustained mixed load") is this step.
+ *   H           device bf16 [batch * (n_draft + 1)][K]: row b * (n_draft + 1)
+ *               + i is sequence b at position i (the last accepted token, then
+ *               its n_draft drafts); batch * (n_draft + 1) <= 32
+ *   W           NVFP4 [V][K], batch 1, ROWMAJOR, K a multiple of 256
+ *   draft_ids   device int32 [batch][n_draft]: the drafted ids; draft i of a
+ *               sequence is checked against the argmax at its position i
+ *   out_tokens  device int32 [batch][n_draft + 1]: the argmax (lowest id among
+ *               equal logits) at every position
+ *   n_accepted  device int32 [batch]: the number of leading drafts equal to
+ *               out_tokens at the same position; the step emits
+ *               out_tokens[b][0 .. n_accepted[b]] (the accepted drafts and one
+ *               token from the target)
+ *   workspace  >= nvfp4_workspace_size(NVFP4_OP_GATHER_ARGMAX, batch * (n_draft + 1), V, K, 0, 0). */
+int nvfp4_verify_accept(const void* H, int64_t batch, int n_draft, nvfp4_tensor_t W, const int32_t* draft_ids,
+                        int32_t* out_tokens, int32_t* n_accepted, void* workspace, size_t workspace_bytes,
+                        nvfp4_stream_t stream);
+
 /* ---- helpers --------------------------------------------------------------- */
 
 /* Bytes of one matrix's block scales in the given layout. */
@@ -255,8 +291,9 @@ size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t c, int64_t e, 
 const char* nvfp4_status_string(int status);
 
 /* Reads and clears the device status word (synchronises `stream`). Bounded
- * on-device waits that give up set NVFP4_ERR_TIMEOUT; nvfp4_gather_rows sets
- * NVFP4_ERR_INVALID_ARG for an index outside the matrix. *out = NVFP4_OK or
+ * on-device waits that give up set NVFP4_ERR_TIMEOUT; nvfp4_gather_rows and
+ * nvfp4_grouped_gemm set NVFP4_ERR_INVALID_ARG for an index outside the
+ * matrix / an expert id outside [0, E). *out = NVFP4_OK or
  * the last status set. */
 int nvfp4_read_device_status(int* out, nvfp4_stream_t stream);
 

@@ -27,7 +27,7 @@ EXPORTS = [
     "nvfp4_moe_route", "nvfp4_grouped_gemm", "nvfp4_gather_gemv_argmax", "nvfp4_gather_rows", "nvfp4_gemv_argmax",
     "nvfp4_scales_bytes", "nvfp4_workspace_size", "nvfp4_status_string",
     "nvfp4_read_device_status", "nvfp4_selftest_bounded_wait", "nvfp4_version",
-    "nvfp4_gemm_w4a16_noalloc",
+    "nvfp4_gemm_w4a16_noalloc", "nvfp4_verify_accept",
 ]
 _NON_INT = ("nvfp4_scales_bytes", "nvfp4_workspace_size", "nvfp4_status_string")
 
@@ -60,6 +60,7 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_gather_gemv_argmax.argtypes = [vp, i64, CTensor, vp, i64, vp, vp, vp, sz, vp]
         L.nvfp4_gather_rows.argtypes = [CTensor, vp, i64, vp, vp, vp]
         L.nvfp4_gemv_argmax.argtypes = [vp, i64, CTensor, vp, vp, vp, vp, sz, vp]
+        L.nvfp4_verify_accept.argtypes = [vp, i64, i32, CTensor, vp, vp, vp, vp, sz, vp]
         L.nvfp4_scales_bytes.argtypes = [i64, i64, i32]
         L.nvfp4_scales_bytes.restype = sz
         L.nvfp4_workspace_size.argtypes = [i32, i64, i64, i64, i64, i64]
@@ -254,6 +255,24 @@ def gemv_argmax(h: torch.Tensor, w: QTensor, ids: torch.Tensor | None = None,
     _check(lib().nvfp4_gemv_argmax(_ptr(h), M, w.c(), _ptr(ids), _ptr(out), _ptr(logit), _ptr(ws), ws.numel(),
                                    _stream()), "nvfp4_gemv_argmax")
     return out, logit
+
+
+def verify_accept(h: torch.Tensor, w: QTensor, draft_ids: torch.Tensor, workspace: torch.Tensor | None = None):
+    """Speculative verify: h bf16 [batch * (n_draft + 1)][K], draft_ids int32
+    [batch][n_draft] -> (argmax ids int32 [batch][n_draft + 1], accepted
+    drafts int32 [batch])."""
+    _require_cuda(h, draft_ids)
+    batch, n_draft = draft_ids.shape
+    if h.shape[0] != batch * (n_draft + 1):
+        raise ValueError("verify_accept: h needs batch * (n_draft + 1) rows")
+    draft_ids = draft_ids.to(torch.int32).contiguous()
+    tokens = torch.empty(batch, n_draft + 1, dtype=torch.int32, device=h.device)
+    n_acc = torch.empty(batch, dtype=torch.int32, device=h.device)
+    ws = workspace if workspace is not None else _workspace(
+        workspace_size(OP_GATHER_ARGMAX, h.shape[0], w.rows, w.K), h.device)
+    _check(lib().nvfp4_verify_accept(_ptr(h), batch, n_draft, w.c(), _ptr(draft_ids), _ptr(tokens), _ptr(n_acc),
+                                     _ptr(ws), ws.numel(), _stream()), "nvfp4_verify_accept")
+    return tokens, n_acc
 
 
 def read_device_status() -> int:

@@ -209,6 +209,22 @@ int nvfp4_gemv_argmax(const void* H, int64_t M, nvfp4_tensor_t W, const int32_t*
                             reinterpret_cast<cudaStream_t>(stream));
 }
 
+int nvfp4_verify_accept(const void* H, int64_t batch, int n_draft, nvfp4_tensor_t W, const int32_t* draft_ids,
+                        int32_t* out_tokens, int32_t* n_accepted, void* workspace, size_t workspace_bytes,
+                        nvfp4_stream_t stream) {
+  if (!H || !out_tokens || !n_accepted || batch < 1 || n_draft < 0 || !tensor_ok(W) || W.batch != 1 || W.rows < 1)
+    return NVFP4_ERR_INVALID_ARG;
+  if (n_draft > 0 && !draft_ids) return NVFP4_ERR_INVALID_ARG;
+  const int64_t M = batch * (n_draft + 1);
+  if (M > 32) return NVFP4_ERR_INVALID_ARG;
+  if (W.scale_layout != NVFP4_SCALES_ROWMAJOR) return NVFP4_ERR_INVALID_ARG;
+  if (W.K % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(H) || !aligned16(W.codes) || !aligned16(W.scales)) return NVFP4_ERR_MISALIGNED;
+  if (!workspace || workspace_bytes < argmax_workspace_bytes(M, W.K)) return NVFP4_ERR_WORKSPACE;
+  return launch_gemv_argmax(static_cast<const uint16_t*>(H), M, W, nullptr, out_tokens, nullptr, workspace,
+                            reinterpret_cast<cudaStream_t>(stream), draft_ids, n_draft, n_accepted);
+}
+
 int nvfp4_read_device_status(int* out, nvfp4_stream_t stream) {
   if (!out) return NVFP4_ERR_INVALID_ARG;
   return read_device_status(out, reinterpret_cast<cudaStream_t>(stream));

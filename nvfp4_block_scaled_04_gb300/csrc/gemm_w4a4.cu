@@ -1,8 +1,8 @@
 // W4A4 NVFP4 GEMM on the 5th-generation tensor cores (sm_103a):
 //   Y[m][n] = bf16( s_tA * s_tW * sum_k a[m][k] * w[n][k] )
-// with a, w the e2m1 * e4m3 block-scaled values - "Blackwell-native NVFP4 W4A4
-// execution" (52.6% More Tokens, 1.53x Less GPU Time: Production Inference
-// with Minima and Rafay). The block-scaled MMA multiplies the e2m1 codes and
+// with a, w the e2m1 * e4m3 block-scaled values: both operands 4-bit, run
+// natively on Blackwell (52.6% More Tokens, 1.53x Less GPU Time: Production
+// Inference with Minima and Rafay, comparison paragraph). The block-scaled MMA multiplies the e2m1 codes and
 // the per-16 E4M3 scales and accumulates in fp32 in tensor memory; the
 // epilogue applies the two fp32 tensor scales and rounds to bf16.
 //

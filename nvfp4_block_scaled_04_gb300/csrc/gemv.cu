@@ -79,13 +79,16 @@ int launch_skinny_nt(int nt, const SkinnyParams& p, dim3 grid, cudaStream_t stre
   }
 }
 
-// Two m-tiles per consumer warp once there are several n-tiles, so each
-// activation fragment read from shared memory feeds two MMAs.
+// One warp layout for every token count: two m-tiles per consumer warp (each
+// activation fragment read from shared memory feeds two MMAs) and the stage's
+// two K-iterations on two warps. A token's output is then summed in the same
+// order whatever the batch size, so its bits do not depend on which other
+// tokens share the call.
 template <int NT>
 int launch_tma_plain_nt(const TmaSkinnyParams& p, const CUtensorMap& mc, const CUtensorMap& ms, dim3 grid,
                         cudaStream_t stream) {
-  constexpr int MT = NT >= 2 ? 2 : 1;
-  constexpr int KW = NT >= 2 ? 2 : 1;   // measured: helps when the MMA work per stage is large
+  constexpr int MT = 2;
+  constexpr int KW = 2;
   auto k = skinny_tma_kernel<NT, SK_PLAIN, MT, KW>;
   int rc = ensure_smem(k, GtCfg<NT>::SMEM);
   if (rc != NVFP4_OK) return rc;
@@ -108,8 +111,11 @@ int launch_tma_argmax_nt(const TmaSkinnyParams& p, const CUtensorMap& mc, const 
 }
 
 // Split-K of the TMA-fed GEMV: as many K-slices per 128-row tile as still fit
-// in one wave of two CTAs per SM (at most 8, at least one stage each).
-int tma_split(int64_t tiles, int64_t n_stages) { return choose_split(tiles, n_stages); }
+// in one wave of two CTAs per SM (at most 8, at least one stage each). It is
+// chosen from the 128-row tiles of ONE token chunk, so it depends on (N, K)
+// alone: a token's partial sums and their reduction order are the same at
+// every M (calls with more than 32 tokens run one such wave per chunk).
+int tma_split(int64_t row_tiles, int64_t n_stages) { return choose_split(row_tiles, n_stages); }
 
 struct DenseWs {
   int* pexp;
@@ -141,9 +147,10 @@ DenseWs carve_dense(void* base, int64_t M, int64_t N, int64_t K, bool argmax) {
   w.pexp = reinterpret_cast<int*>(b + off);
   off += align_up(static_cast<size_t>(chunks) * GV_MCHUNK * sizeof(int));
   if (!argmax && K % 256 == 0) {
-    // only a split tile needs counters and partials; then tiles * split <= 2 * SMs
+    // only a split tile needs counters and partials; then per token chunk
+    // row tiles * split <= 2 * SMs
     const int64_t tiles = chunks * ceil_div(N, GV_ROWS);
-    const int S = tma_split(tiles, K / 256);
+    const int S = tma_split(ceil_div(N, GV_ROWS), K / 256);
     if (S > 1) {
       w.n_tile_counters = static_cast<int>(tiles);
       w.tile_counters = reinterpret_cast<unsigned int*>(b + off);
@@ -193,7 +200,7 @@ int launch_gemm_w4a16(const uint16_t* X, int64_t M, const nvfp4_tensor_t& W, uin
     q.xfrag = w.xfrag;
     q.pexp = w.pexp;
     q.M = M;
-    q.split = tma_split(row_tiles * chunks, n_it / 2);
+    q.split = tma_split(row_tiles, n_it / 2);
     q.Y = Y;
     q.status = device_status_ptr();
     q.partials = w.partials;
@@ -215,7 +222,7 @@ int launch_gemm_w4a16(const uint16_t* X, int64_t M, const nvfp4_tensor_t& W, uin
   p.xfrag = w.xfrag;
   p.pexp = w.pexp;
   p.M = M;
-  p.split = choose_split(row_tiles * chunks, n_it);
+  p.split = choose_split(row_tiles, n_it);   // from (N, K) alone, as for the TMA-fed kernel
   p.Y = Y;
   dim3 grid(static_cast<unsigned>(p.split), static_cast<unsigned>(row_tiles), static_cast<unsigned>(chunks));
   return launch_skinny_nt<SK_PLAIN>(nt, p, grid, stream);
@@ -231,9 +238,11 @@ int launch_gather_rows(const nvfp4_tensor_t& W, const int32_t* idx, int64_t n_id
 }
 
 // GEMV + argmax over every row of W (consecutive rows through 2-D TMA boxes);
-// row j is reported as ids[j] (j when ids is null).
+// row j is reported as ids[j] (j when ids is null). With n_accepted the call
+// is a speculative verify head (see TmaSkinnyParams).
 int launch_gemv_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, const int32_t* ids,
-                       int32_t* out_ids, float* out_logit, void* ws, cudaStream_t stream) {
+                       int32_t* out_ids, float* out_logit, void* ws, cudaStream_t stream,
+                       const int32_t* draft_ids, int n_draft, int32_t* n_accepted) {
   const int64_t K = W.K;
   const DenseWs w = carve_dense(ws, M, 0, K, true);   // keys and counter zeroed by the prep kernel
   const int nt = static_cast<int>(ceil_div(M, 8));
@@ -258,6 +267,9 @@ int launch_gemv_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, co
   q.counter = w.counter;
   q.out_ids = out_ids;
   q.out_logit = out_logit;
+  q.draft_ids = draft_ids;
+  q.n_draft = n_draft;
+  q.n_accepted = n_accepted;
   const dim3 grid(1, static_cast<unsigned>(ceil_div(W.rows, GV_ROWS)), 1);
   switch (nt) {
     case 1: return launch_tma_argmax_nt<1, false>(q, mc, ms, grid, stream);

@@ -86,6 +86,13 @@ struct TmaSkinnyParams {
   float* out_logit;            // nullable
   const uint8_t* codes;        // row-streaming ARGMAX: the weight itself
   const uint8_t* scales;
+  // ARGMAX as a speculative verify head (n_accepted non-null): the M rows are
+  // `M / (n_draft + 1)` sequences of n_draft + 1 positions; the finishing CTA
+  // also counts, per sequence, the leading drafts equal to the argmax at
+  // their position
+  const int32_t* draft_ids;    // [M / (n_draft + 1)][n_draft]
+  int n_draft;
+  int32_t* n_accepted;         // [M / (n_draft + 1)]
 };
 
 // MMA row g of a warp's 16-row tile reads shared-memory row sigma(g) (and
@@ -482,6 +489,17 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
           if (p.out_logit) p.out_logit[m] = float_from_order_key(static_cast<uint32_t>(key >> 32));
         }
         if (tid == 0) atomicExch(p.counter, 0u);
+        if (p.n_accepted) {
+          // greedy acceptance: the drafts of a sequence are accepted up to the
+          // first one that differs from the argmax at its position
+          __syncthreads();   // this CTA's writes of out_ids are visible to it
+          const int d1 = p.n_draft + 1;
+          for (int b = tid; b < static_cast<int>(p.M) / d1; b += NTHR) {
+            int n = 0;
+            while (n < p.n_draft && p.draft_ids[b * p.n_draft + n] == p.out_ids[b * d1 + n]) ++n;
+            p.n_accepted[b] = n;
+          }
+        }
       }
     }
   } else if (MODE == SK_PLAIN) {

@@ -86,7 +86,8 @@ int launch_gather_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, 
 int launch_gather_rows(const nvfp4_tensor_t& W, const int32_t* idx, int64_t n_idx, uint8_t* codes_out,
                        uint8_t* scales_out, cudaStream_t stream);
 int launch_gemv_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, const int32_t* ids,
-                       int32_t* out_ids, float* out_logit, void* ws, cudaStream_t stream);
+                       int32_t* out_ids, float* out_logit, void* ws, cudaStream_t stream,
+                       const int32_t* draft_ids = nullptr, int n_draft = 0, int32_t* n_accepted = nullptr);
 
 // ---- moe.cu
 int launch_moe_route(const float* logits, int64_t T, int E, int topk, int32_t* ids, float* weights,

@@ -131,13 +131,15 @@ constexpr int XT_MIN_ROWS_PER_EXPERT = 32;
 // tensor-core tiles (each expert's rows in tiles of up to XT_NMAX) with a
 // block scan, write the chunk and tile tables and row_of = -1, then hand out
 // each routed row's position within its expert (shared atomics again).
-// Replaces a memset and three kernels (count, plan, scatter).
+// Replaces a memset and three kernels (count, plan, scatter). A routed slot
+// whose expert id lies outside [0, E) gets no row (pos_of = -1, so it
+// contributes nothing) and sets NVFP4_ERR_INVALID_ARG in the status word.
 constexpr int PLAN_THREADS = 1024;
 __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t* ids, int64_t R, int topk, int E,
                                                                   int* poff, int* chunk_count, int* chunk_expert,
                                                                   int* chunk_rows, int* tile_count, int* tile_expert,
                                                                   int* tile_row0, int* tile_rows, int* row_of,
-                                                                  int* pos_of) {
+                                                                  int* pos_of, int* status) {
   __shared__ int s_cnt[PLAN_MAX_E];
   __shared__ int s_off[PLAN_MAX_E];
   __shared__ int s_wr[PLAN_THREADS / 32], s_wt[PLAN_THREADS / 32];
@@ -219,14 +221,15 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int64_t i = i0 + u * PLAN_THREADS;
-      ev[u] = i < R ? ids[i] : -2;
+      ev[u] = i < R ? ids[i] : 0;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int64_t i = i0 + u * PLAN_THREADS;
-      if (ev[u] == -2) continue;
+      if (i >= R) continue;
       if (ev[u] < 0 || ev[u] >= E) {
         pos_of[i] = -1;
+        atomicExch(status, NVFP4_ERR_INVALID_ARG);
         continue;
       }
       const int pos = s_off[ev[u]] + atomicAdd(&s_cnt[ev[u]], 1);
@@ -480,7 +483,7 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
   const MoeWs m = carve_moe(ws, T, H, I, E, topk);
   route_plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.chunk_count,
                                             m.chunk_expert, m.chunk_rows, m.tile_count, m.tile_expert, m.tile_row0,
-                                            m.tile_rows, m.row_of, m.pos_of);
+                                            m.tile_rows, m.row_of, m.pos_of, device_status_ptr());
   int rc = from_cuda(cudaGetLastError());
   if (rc != NVFP4_OK) return rc;
 

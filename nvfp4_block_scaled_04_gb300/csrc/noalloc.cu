@@ -20,7 +20,16 @@
 //     results; serialise them. Each call rewrites every byte it later reads,
 //     so nothing has to start at zero.
 //   - Limits: 1 <= M <= 32 tokens and K <= 32768; larger shapes are rejected
-//     with NVFP4_ERR_SCRATCH_LIMIT before anything is launched.
+//     with NVFP4_ERR_SCRATCH_LIMIT before anything is launched. Within them
+//     the scratch a call needs is the split-K partials (one 32 x 128 fp32
+//     block per CTA, at most two CTAs per SM: 4.75 MiB on 152 SMs) plus the
+//     f16 activation fragments (2 MiB at K = 32768) and a few KiB of shifts
+//     and counters, under the 8 MiB of the array; the size is checked on
+//     every call, so a GPU with more SMs gets the error rather than an
+//     overrun.
+//   - The cached address belongs to the device's current module image:
+//     after cudaDeviceReset it is stale, so the library must not be used on
+//     a device after a reset in the same process.
 #include <mutex>
 
 #include "common.cuh"

@@ -7,9 +7,9 @@
 //   sb    = amax_block / (s_t * 6) -> E4M3, nearest even, saturating at 448
 //   q     = x / (e4m3(sb) * s_t)   -> e2m1, nearest even, saturating at 6
 // with the sign bit of x kept on codes whose magnitude rounds to zero, and a
-// zero block scale forcing zero codes. Format: "NVFP4 is 4-bit e2m1 with
-// per-16 FP8 scales" (Serving Qwen3.8-27B in 4-bit with a masked speculative
-// decoding head, "What the artifact is").
+// zero block scale forcing zero codes. Format: 4-bit e2m1 values with one
+// 8-bit float scale per 16 elements (Serving Qwen3.8-27B in 4-bit with a
+// masked speculative decoding head, "What the artifact is").
 #include "common.cuh"
 #include "launch.h"
 

@@ -6,23 +6,24 @@ CPU-baseline / reference legs use it. It shares no code with the CUDA path.
 
 What it computes, and the passages it follows
 ---------------------------------------------
-* The format: "NVFP4 is 4-bit e2m1 with per-16 FP8 scales"
-  (Serving Qwen3.8-27B in 4-bit with a masked speculative decoding head,
-  "What the artifact is"). The FP8 scale is E4M3, "an eight-bit float with
-  four exponent bits and three mantissa bits" (What 350+ Experiments Taught Us
-  About Serving Qwen 3.6 35B-A3B, section 3 "KV cache and memory capacity").
+* The format: 4-bit e2m1 values, one 8-bit float scale per 16 consecutive
+  elements (Serving Qwen3.8-27B in 4-bit with a masked speculative decoding
+  head, "What the artifact is"). That scale is E4M3, an 8-bit float with 4
+  exponent and 3 mantissa bits (What 350+ Experiments Taught Us About Serving
+  Qwen 3.6 35B-A3B, section 3 "KV cache and memory capacity").
   A second, FP32 per-tensor scale multiplies every decoded value.
-* W4A16: "four-bit weights and 16-bit activations" (What 350+ Experiments...,
+* W4A16: 4-bit weights against 16-bit activations (What 350+ Experiments...,
   section 1 "Checkpoint packages and quantisation"; Qwen3.8-27B benchmark,
   "Serving configuration measured").
-* W4A4: "Blackwell-native NVFP4 W4A4 execution" (52.6% More Tokens, 1.53x Less
-  GPU Time: Production Inference with Minima and Rafay, comparison paragraph).
-* Routed-expert MoE layer (What 350+ Experiments..., section 1 and section 7
-  "FlashInfer CUTLASS for NVFP4 mixture-of-experts operations").
+* W4A4: both operands NVFP4, run natively on Blackwell (52.6% More Tokens,
+  1.53x Less GPU Time: Production Inference with Minima and Rafay, comparison
+  paragraph).
+* Routed-expert MoE layer (What 350+ Experiments..., section 1 and section 7,
+  where the final configuration runs the expert GEMMs on an NVFP4 MoE kernel).
 * Masked draft LM head: the draft proposes only ids from a fixed 32,768-id
   subset of the 248,320-row head; verification stays full-vocabulary, so the
-  mask "can never change output" (Serving Qwen3.8-27B..., "The masked head
-  trick").
+  mask cannot alter what the model emits (Serving Qwen3.8-27B..., "The masked
+  head trick").
 
 Readings where the pages are silent (each is listed in the design doc):
   R1 tensor scale  s_t = amax(|x|) / 2688 in fp32 (2688 = 6 * 448); s_t = 1
@@ -44,6 +45,11 @@ Readings where the pages are silent (each is listed in the design doc):
      W13 rows [0, I) are the gate, [I, 2I) the up projection;
      h = bf16(silu(g) * u); out = sum_j w_j * (h_j @ W2_e^T).
      Each expert matrix carries its own tensor scale.
+  R11 verify       speculative verification is greedy: sequence b's rows
+     are its n_draft + 1 positions; the target token at position i is the
+     full-vocabulary argmax there (R6); the drafts are accepted up to the
+     first one that differs from the target token at its position, and the
+     step emits the accepted drafts plus the target token after them.
   R10 W4A4 MoE     (the routed experts with 4-bit activations as well): the
      layer input is quantised once per call with its own dynamic tensor scale
      and each routed row is its token's quantised row; h as in R7; the h rows
@@ -274,6 +280,31 @@ def top2_margin(logits):
     return (s[:, -1] - s[:, -2]) / rms
 
 
+def accept_greedy(target_ids, draft_ids):
+    """R11: per sequence, the number of leading drafts equal to the target
+    token at the same position. target_ids [B][D+1], draft_ids [B][D]."""
+    target_ids = np.asarray(target_ids, dtype=np.int64)
+    draft_ids = np.asarray(draft_ids, dtype=np.int64)
+    B, D = draft_ids.shape
+    n = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        while n[b] < D and draft_ids[b, n[b]] == target_ids[b, n[b]]:
+            n[b] += 1
+    return n
+
+
+def verify_accept(h, w: QTensor, draft_ids):
+    """Speculative verify step (R11): full-vocabulary logits of the
+    B * (D + 1) hidden rows, the target token per position (R6), and the
+    accepted draft count per sequence. Returns (target ids [B][D+1], accepted
+    [B], logits [B*(D+1)][V])."""
+    draft_ids = np.asarray(draft_ids, dtype=np.int64)
+    B, D = draft_ids.shape
+    ids, _, logits = gather_gemv_argmax(h, w, None)
+    target = ids.reshape(B, D + 1)
+    return target, accept_greedy(target, draft_ids), logits
+
+
 # ---------------------------------------------------------------------------
 # Routed-expert MoE layer.
 # ---------------------------------------------------------------------------
@@ -295,7 +326,8 @@ def moe_route(logits, topk):
 
 def silu(g):
     g = np.asarray(g, dtype=np.float64)
-    return g / (1.0 + np.exp(-g))
+    with np.errstate(over="ignore"):   # exp(-g) = inf for g << 0 gives the right limit, 0
+        return g / (1.0 + np.exp(-g))
 
 
 def moe_forward(x, ids, weights, w13: list, w2: list):

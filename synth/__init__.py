@@ -97,9 +97,24 @@ def prefill_inputs(M: int = 8192, K: int = HIDDEN_27B, N: int = GATE_UP_27B):
     return student_t_bf16((M, K), 4, seed=3), normal_f32((N, K), 0.02, seed=4)
 
 
+HEAD_BLOCK = 4096            # rows of the draft head drawn per seed
+
+
+def draft_head_blocks(V: int = VOCAB) -> int:
+    return (V + HEAD_BLOCK - 1) // HEAD_BLOCK
+
+
+def draft_head_block(b: int, V: int = VOCAB, K: int = HIDDEN_27B) -> torch.Tensor:
+    """Rows [4096 b, min(4096 (b + 1), V)) of the LM-head weight, fp32
+    N(0, 0.02^2), seed 5_000_000 + b: every block has its own generator, so a
+    worker process can redraw any block without the others."""
+    r0 = b * HEAD_BLOCK
+    return normal_f32((min(HEAD_BLOCK, V - r0), K), 0.02, seed=5_000_000 + b)
+
+
 def draft_head_weight(V: int = VOCAB, K: int = HIDDEN_27B) -> torch.Tensor:
-    """LM-head weight fp32 N(0, 0.02^2) [V][K], seed 5."""
-    return normal_f32((V, K), 0.02, seed=5)
+    """LM-head weight fp32 N(0, 0.02^2) [V][K]: the blocks of draft_head_block."""
+    return torch.cat([draft_head_block(b, V, K) for b in range(draft_head_blocks(V))])
 
 
 def draft_mask(V: int = VOCAB, n: int = MASK_ROWS) -> torch.Tensor:
@@ -110,6 +125,12 @@ def draft_mask(V: int = VOCAB, n: int = MASK_ROWS) -> torch.Tensor:
 def draft_hidden(M: int, step: int, K: int = HIDDEN_27B) -> torch.Tensor:
     """bf16 N(0,1) draft-head hidden states [M][K] for draft step `step`."""
     return normal_bf16((M, K), seed=7 + step)
+
+
+def verify_hidden(M: int = 32, K: int = HIDDEN_27B) -> torch.Tensor:
+    """bf16 N(0,1) hidden states of a speculative verify batch [M][K] (seed 20):
+    batch x (drafts + 1) positions, at most 32 rows."""
+    return normal_bf16((M, K), seed=20)
 
 
 def moe_inputs(T: int, E: int = MOE_EXPERTS, H: int = MOE_HIDDEN, I: int = MOE_INTER):

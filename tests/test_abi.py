@@ -123,6 +123,20 @@ def test_row_gather_and_compact_argmax_validate_arguments(nv):
     assert L.nvfp4_gemv_argmax(_fake(), 1, W, None, _fake(), None, None, 0, None) == -5       # workspace
 
 
+def test_verify_accept_validates_arguments(nv):
+    L = nv.lib()
+    ws = _fake()
+    W = nv.CTensor(0x1000, 0x2000, 0x3000, 64, 256, 1, 0)
+    ok = (_fake(), 4, 3, W, _fake(), _fake(), _fake(), ws, 1 << 20, None)
+    assert L.nvfp4_verify_accept(_fake(), 9, 3, W, _fake(), _fake(), _fake(), ws, 1 << 20, None) == -1  # 36 rows
+    assert L.nvfp4_verify_accept(_fake(), 4, 3, W, None, _fake(), _fake(), ws, 1 << 20, None) == -1    # no drafts
+    assert L.nvfp4_verify_accept(_fake(), 0, 3, W, _fake(), _fake(), _fake(), ws, 1 << 20, None) == -1  # batch
+    Wa = nv.CTensor(0x1000, 0x2000, 0x3000, 64, 384, 1, 0)
+    assert L.nvfp4_verify_accept(_fake(), 4, 3, Wa, _fake(), _fake(), _fake(), ws, 1 << 20, None) == -2  # K % 256
+    assert L.nvfp4_verify_accept(_fake(0x1008), *ok[1:]) == -3                                          # H misaligned
+    assert L.nvfp4_verify_accept(*ok[:7], None, 0, None) == -5                                          # workspace
+
+
 def test_grouped_gemm_validates_arguments(nv):
     L = nv.lib()
     ws = _fake(0x20000)

@@ -79,11 +79,43 @@ def _compact():
     return nv().gather_rows(qw, idx.to(DEV))
 
 
+@functools.lru_cache(maxsize=1)
+def _full_vocab_oracle():
+    """The oracle's fp64 logits over all 248,320 head rows for the hidden
+    states of the full-vocabulary checks: the 8-row hidden states of draft
+    steps 0..2 (M = 1 and 4 are their first rows) and the 32-row verify batch.
+    Returns {key: logits [rows][V]}."""
+    from tests.head_oracle import full_head_logits
+    _, _, _, st, _ = _head()
+    hs = [synth.draft_hidden(8, s).float().numpy() for s in range(3)] + [synth.verify_hidden(32).float().numpy()]
+    lg = full_head_logits(np.concatenate(hs), st)
+    out = {("draft", s): lg[8 * s:8 * s + 8] for s in range(3)}
+    out["verify"] = lg[24:56]
+    return out
+
+
+def check_full_vocab(ids, logit, logits):
+    """The spec rule over every row of the head: the GPU id equals the
+    oracle's (lowest id among equal maxima) wherever the oracle's top-2 margin
+    exceeds the tolerance, and is one of the top two otherwise; its logit
+    matches the oracle's maximum."""
+    rows = np.arange(logits.shape[1])
+    oid, omax = O.argmax_lowest_id(logits, rows)
+    margin = O.top2_margin(logits)
+    for r in range(len(ids)):
+        rms = np.sqrt(np.mean(logits[r] ** 2))
+        if margin[r] > TOL:
+            assert int(ids[r]) == int(oid[r]), (r, margin[r])
+        else:
+            assert int(ids[r]) in set(np.argsort(logits[r])[-2:].tolist())
+        assert abs(float(logit[r]) - omax[r]) <= TOL * rms
+
+
 @pytest.mark.parametrize("M", [1, 4, 8])
 def test_draft_head_config(M):
     """248,320 x 5120 head, 32,768-id mask, 3 draft steps: the masked argmax
-    is checked exactly against the oracle over all masked rows; the full-vocab
-    argmax is checked by its value and by sampled rows."""
+    is checked exactly against the oracle over all masked rows, and the
+    full-vocabulary argmax over all 248,320 rows."""
     m = nv()
     w, idx, qw, st, wq_masked = _head()
     idx_np = idx.numpy()
@@ -104,16 +136,26 @@ def test_draft_head_config(M):
                 if margin[r] > TOL:
                     assert logits[r][pos] == omax[r]
                 assert abs(lg - omax[r]) <= TOL * rms
-    # full vocabulary: the winner's oracle logit matches and no sampled row beats it
-    h = synth.draft_hidden(M, 0)
-    ids, logit = m.gather_gemv_argmax(h.to(DEV), qw, None)
-    rows = np.random.default_rng(5).choice(w.shape[0], 8192, replace=False)
-    for r in range(M):
-        cand = np.concatenate([rows, [int(ids[r])]])
-        lg, _ = O.gather_logits(h.float().numpy()[r:r + 1], O.quantize(w.numpy()[cand], s_t=st), None)
-        rms = np.sqrt(np.mean(lg ** 2))
-        assert abs(lg[0, -1] - float(logit[r])) <= TOL * rms
-        assert lg[0].max() <= float(logit[r]) + TOL * rms
+    # full vocabulary, every row of the head
+    full = _full_vocab_oracle()
+    for step in range(3):
+        h = synth.draft_hidden(M, step)
+        ids, logit = m.gather_gemv_argmax(h.to(DEV), qw, None)
+        check_full_vocab(ids.cpu().numpy(), logit.cpu().numpy(), full[("draft", step)][:M])
+
+
+def test_verify_head_full_vocab_m32():
+    """The speculative verify shape: 32 rows (batch x (drafts + 1)) against
+    the full 248,320-row head, through both entry points, checked over every
+    row of the head."""
+    m = nv()
+    _, _, qw, _, _ = _head()
+    h = synth.verify_hidden(32).to(DEV)
+    full = _full_vocab_oracle()["verify"]
+    ids, logit = m.gemv_argmax(h, qw, None)
+    check_full_vocab(ids.cpu().numpy(), logit.cpu().numpy(), full)
+    ids_g, logit_g = m.gather_gemv_argmax(h, qw, None)
+    check_full_vocab(ids_g.cpu().numpy(), logit_g.cpu().numpy(), full)
 
 
 def test_gather_rows_matches_the_oracles_rows_byte_for_byte():
@@ -156,3 +198,61 @@ def test_gather_rows_out_of_range_index_is_reported():
     sub = m.gather_rows(qw, idx)
     assert m.read_device_status() == m.ERR_INVALID_ARG
     assert int(sub.codes[1].abs().sum()) == 0 and torch.equal(sub.codes[0], qw.codes[3])
+
+
+def _drafts_from(target, V):
+    """Drafts built from the oracle's own target tokens: sequence b gets its
+    first b % (D + 1) drafts right and the next one wrong, so every accepted
+    length 0..D occurs."""
+    B, D1 = target.shape
+    drafts = target[:, :D1 - 1].copy()
+    for b in range(B):
+        k = b % D1
+        if k < D1 - 1:
+            drafts[b, k] = (drafts[b, k] + 1) % V
+    return drafts
+
+
+def check_verify(tokens, n_acc, drafts, logits):
+    B, D1 = tokens.shape
+    V = logits.shape[1]
+    oid, _ = O.argmax_lowest_id(logits, np.arange(V))
+    target = oid.reshape(B, D1)
+    n_ref = O.accept_greedy(target, drafts)
+    margin = O.top2_margin(logits).reshape(B, D1)
+    for b in range(B):
+        # the count follows the returned tokens (greedy acceptance)
+        assert int(n_acc[b]) == int(O.accept_greedy(tokens[b:b + 1], drafts[b:b + 1])[0])
+        for i in range(D1):
+            if margin[b, i] > TOL:
+                assert int(tokens[b, i]) == int(target[b, i]), (b, i)
+        if all(margin[b, i] > TOL for i in range(min(int(n_ref[b]), D1 - 1) + 1)):
+            assert int(n_acc[b]) == int(n_ref[b]), b
+
+
+@pytest.mark.parametrize("B,D", [(1, 0), (2, 3), (4, 7), (8, 3), (32, 0)])
+def test_verify_accept_small_head(B, D):
+    m = nv()
+    V, K = 3000, 512
+    w = synth.normal_f32((V, K), 0.02, seed=91)
+    h = synth.normal_bf16((B * (D + 1), K), seed=92 + B)
+    wq = O.quantize(w.numpy())
+    ids, _, logits = O.gather_gemv_argmax(h.float().numpy(), wq, None)
+    drafts = _drafts_from(ids.reshape(B, D + 1), V)
+    tokens, n_acc = m.verify_accept(h.to(DEV), m.quantize(w.to(DEV)),
+                                    torch.from_numpy(drafts.astype(np.int32)).to(DEV))
+    check_verify(tokens.cpu().numpy(), n_acc.cpu().numpy(), drafts, logits)
+
+
+def test_verify_accept_full_size():
+    """Speculative verify at the 248,320 x 5120 head: 8 sequences x (3 drafts
+    + 1) = 32 rows, every accepted length 0..3, against the oracle's logits
+    over every row of the head."""
+    m = nv()
+    _, _, qw, _, _ = _head()
+    logits = _full_vocab_oracle()["verify"]
+    oid, _ = O.argmax_lowest_id(logits, np.arange(logits.shape[1]))
+    drafts = _drafts_from(oid.reshape(8, 4), logits.shape[1])
+    tokens, n_acc = m.verify_accept(synth.verify_hidden(32).to(DEV), qw,
+                                    torch.from_numpy(drafts.astype(np.int32)).to(DEV))
+    check_verify(tokens.cpu().numpy(), n_acc.cpu().numpy(), drafts, logits)

@@ -154,3 +154,32 @@ def test_moe_config_t4096_sampled_tokens():
                         [r13.get(e, r13[used[0]]) for e in range(128)],
                         [r2.get(e, r2[used[0]]) for e in range(128)])
     assert O.rel_fro(out[toks], ref) <= TOL
+
+
+@pytest.mark.parametrize("T,E,H,I", [(40, 8, 128, 128), (512, 4, 256, 256)])
+def test_out_of_range_expert_ids_are_dropped_and_reported(T, E, H, I):
+    """Slots whose expert id is -2, -1 or E contribute nothing, and the call
+    reports NVFP4_ERR_INVALID_ARG in the device status word; the result equals
+    the layer with those slots' weights set to zero. (512, 4, 256, 256) runs the
+    tensor-core path."""
+    m = nv()
+    k = 2
+    logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=T + 7)
+    ids, wts = m.moe_route(logits.to(DEV), k)
+    bad = ids.clone()
+    bad[0, 0], bad[3, 1], bad[T - 1, 0] = -2, -1, E
+    dropped = wts.clone()
+    dropped[0, 0], dropped[3, 1], dropped[T - 1, 0] = 0.0, 0.0, 0.0
+    m.read_device_status()   # clear
+    out, _, _ = run_gpu(logits, x, w13, w2, k, bad, wts)
+    assert m.read_device_status() == m.ERR_INVALID_ARG
+    assert np.all(np.isfinite(out))
+    ref_ids = bad.cpu().numpy()
+    ref = O.moe_forward(x.float().numpy(), ref_ids, dropped.cpu().numpy().astype(np.float64),
+                        [O.quantize(t.numpy()) for t in w13], [O.quantize(t.numpy()) for t in w2])
+    assert O.rel_fro(out, ref) <= TOL
+    # the same as routing those slots to a real expert with weight zero
+    ok_ids = ids.clone()
+    clean, _, _ = run_gpu(logits, x, w13, w2, k, ok_ids, dropped)
+    assert m.read_device_status() == m.OK
+    assert O.rel_fro(out, clean) <= TOL

@@ -122,3 +122,24 @@ def test_activation_magnitude_changes_along_k(N, K):
     assert np.all(y[4] == 0.0)
     for r in (0, 1, 2, 3, 5, 6):
         assert O.rel_fro(y[r], ref[r]) <= TOL, r
+
+
+@pytest.mark.parametrize("N,K", [(1000, 2048), (5120, 17408), (300, 384), (34816, 5120)])
+def test_token_bits_do_not_depend_on_batch(N, K):
+    """Every fast path gated byte-identical to plain decode (Serving
+    Qwen3.8-27B..., "Rules I learned the expensive way"): one token's output
+    row is bit for bit the same whether it runs alone or inside batches of 8,
+    17, 32 (the shape buckets of decode), 33 or 70 tokens (several token
+    chunks), at a split-K shape (17408 -> 5120), a single-pass one (5120 ->
+    34816) and the register-fed kernel (K = 384)."""
+    m = nv()
+    qw = m.quantize(synth.normal_f32((N, K), 0.02, seed=N + 3 * K).to(DEV))
+    tok = synth.normal_bf16((1, K), seed=K + 1).to(DEV)
+    rows = []
+    for M in (1, 8, 17, 32, 33, 70):
+        x = synth.normal_bf16((M, K), seed=M + 100).to(DEV)
+        pos = M - 1                        # the last row: another token chunk once M > 32
+        x[pos] = tok[0]
+        rows.append(m.gemm_w4a16(x, qw)[pos].clone())
+    for M, r in zip((8, 17, 32, 33, 70), rows[1:]):
+        assert torch.equal(r.view(torch.int16), rows[0].view(torch.int16)), M

@@ -353,6 +353,31 @@ def test_masked_head_planted_winner():
     assert ids[0] == target
 
 
+def test_greedy_acceptance_hand_cases():
+    # target tokens per position, drafts per position (R11): accept up to the first mismatch
+    target = np.array([[5, 7, 9, 2], [5, 7, 9, 2], [1, 1, 1, 1], [4, 0, 0, 0]])
+    drafts = np.array([[5, 7, 9], [5, 8, 9], [2, 1, 1], [4, 0, 0]])
+    np.testing.assert_array_equal(O.accept_greedy(target, drafts), [3, 1, 0, 3])
+    # no drafts: every sequence emits just the target token
+    np.testing.assert_array_equal(O.accept_greedy(target[:, :1], np.zeros((4, 0), dtype=np.int64)), [0, 0, 0, 0])
+
+
+def test_verify_accept_drafts_equal_to_the_targets_are_all_accepted():
+    wq, rng = _small_head(seed=21)
+    B, D = 3, 4
+    h = rng.standard_normal((B * (D + 1), 64))
+    ids, _, _ = O.gather_gemv_argmax(h, wq, None)
+    target = ids.reshape(B, D + 1)
+    drafts = target[:, :D].copy()
+    # sequence 1: the third draft is wrong; sequence 2: the first one
+    drafts[1, 2] = (drafts[1, 2] + 1) % wq.shape[0]
+    drafts[2, 0] = (drafts[2, 0] + 5) % wq.shape[0]
+    t, n, logits = O.verify_accept(h, wq, drafts)
+    np.testing.assert_array_equal(t, target)
+    np.testing.assert_array_equal(n, [D, 2, 0])
+    assert logits.shape == (B * (D + 1), wq.shape[0])
+
+
 def test_masked_read_ratio_is_the_pages_7_6x():
     # same bytes per row for every row, so the read shrinks by V / n_idx
     assert round(248320 / 32768, 1) == 7.6
