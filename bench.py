@@ -187,32 +187,42 @@ def l2_flush(flush):
     clean.sum()
 
 
-def time_graph(g, reps, warmup=3, flush=None):
-    """Mean ms per replay. With `flush`, L2 is flushed before every replay and
-    only the replay is timed (the flush keeps the GPU busy while the replay is
-    enqueued, so no launch gap enters the timing)."""
+def time_graph(g, reps, warmup=5, flush=None):
+    """Median ms per replay over `reps` replays, each bracketed by its own CUDA
+    events on the launching stream, after `warmup` untimed replays. With
+    `flush`, L2 is flushed before every replay and only the replay is timed
+    (the flush keeps the GPU busy while the replay is enqueued, so no launch
+    gap enters the timing)."""
     import torch
     for _ in range(warmup):
         g.replay()
     torch.cuda.synchronize()
-    if flush is None:
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
-            g.replay()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / reps
-    total = 0.0
-    for _ in range(reps):
-        l2_flush(flush)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        if flush is not None:
+            l2_flush(flush)
         a.record()
         g.replay()
         b.record()
-        torch.cuda.synchronize()
-        total += a.elapsed_time(b)
-    return total / reps
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+def time_graph_mean(g, reps, warmup=5):
+    """Mean ms per replay of `reps` back-to-back replays between two events
+    (graphs whose replays are chained by programmatic dependent launch, whose
+    overlap a per-replay event pair would break)."""
+    import torch
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
 
 
 # sources of the dominant decode kernel; the committed DRAM-traffic record is
@@ -338,6 +348,20 @@ def measure_rows(nv, peaks, reps):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
 
+    # the FP4 tensor pipe's own ceiling: one CTA per SM issuing block-scaled
+    # 128 x 256 x 64 MMAs from shared memory, no global traffic
+    n_mma = 20000
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    gp = capture(lambda: nv.probe_fp4_mma_rate(n_mma))
+    clk = ClockSampler(torch.cuda.current_device()).start()
+    tp = time_graph(gp, reps)
+    ck = clk.stop()
+    probe_tflops = sms * n_mma * 2.0 * 128 * 256 * 64 / tp / 1e9
+    out["fp4_ceiling_measured"] = {"tflops": probe_tflops, "ms": tp, "ctas": sms, "mma_per_cta": n_mma,
+                                   "instruction": "tcgen05.mma.cta_group::1.kind::mxf4nvf4 128x256x64",
+                                   "sm_mhz_median": ck["sm_mhz"], "clock_reasons": ck["reasons"]}
+    del gp
+
     # prefill W4A4, M=8192 K=5120 N=34816
     M, K, N = 8192, 5120, 34816
     a = gpu_student_t((M, K), 4, seed=3)
@@ -361,6 +385,7 @@ def measure_rows(nv, peaks, reps):
     out["w4a4_prefill"] = {
         "shape": [M, N, K], "ms": t, "tflops": flops / t / 1e9, "frac_fp4_peak": flops / t / 1e9 / fp4_peak,
         "fp4_peak_tflops": fp4_peak, "peak_basis": f"{peaks['source']} bf16 x {FP4_OVER_BF16:g}",
+        "frac_fp4_ceiling_measured": flops / t / 1e9 / probe_tflops,
         "ms_with_quantize": t2, "tflops_with_quantize": flops / t2 / 1e9}
     qbytes = M * K * 2 + M * K // 2 + M * K // 16
     out["quantize_activations"] = {"shape": [M, K], "ms": tq, "gbs": qbytes / tq / 1e6,
@@ -406,6 +431,18 @@ def measure_rows(nv, peaks, reps):
     head["bytes_ratio_full_over_masked"] = V / 32768
     head["timing"] = "per draft step: graphs of 3 steps (one mask and hidden state each), L2 flushed per graph"
     out["draft_head"] = head
+
+    # speculative verify: 8 sequences x (3 drafts + 1) = 32 rows against the
+    # full vocabulary, greedy acceptance fused into the argmax's last CTA
+    B, D = 8, 3
+    hv = [gpu_normal((B * (D + 1), K), 1.0, seed=40 + s, dtype=torch.bfloat16) for s in range(3)]
+    drafts = torch.randint(0, V, (B, D), generator=gperm, device="cuda", dtype=torch.int64).to(torch.int32)
+    wsv = torch.zeros(nv.workspace_size(nv.OP_GATHER_ARGMAX, B * (D + 1), V, K), dtype=torch.uint8, device="cuda")
+    g = capture(lambda: [nv.verify_accept(hv[s], qh, drafts, workspace=wsv) for s in range(3)])
+    t = time_graph(g, reps, flush=flush) / 3
+    b = V * (K // 2 + K // 16) + 2 * B * (D + 1) * K
+    out["verify_head"] = {"rows": B * (D + 1), "ms": t, "gbs": b / t / 1e6, "frac_hbm": b / t / 1e6 / peaks["hbm_gbs"],
+                          "timing": "per verify step: graphs of 3 steps, L2 flushed per graph"}
     del qh, qmasks
     torch.cuda.empty_cache()
 
@@ -435,59 +472,118 @@ def measure_rows(nv, peaks, reps):
 
 
 # ------------------------------------------------------------- CPU oracle
+#
+# The oracle (numpy) runs in child processes started with OMP_NUM_THREADS,
+# OPENBLAS_NUM_THREADS and MKL_NUM_THREADS set to 1, so each child computes on
+# exactly one core: one child alone gives the single-core figure, one child
+# per available host core (each on its own sample of weight rows, all at
+# once) the all-core figure. The decode weights are drawn once by the parent
+# and shared with the children through memory-mapped .npy files.
 
-_ORACLE_W = {}
-
-
-def _oracle_weights():
-    """The decode weights on the host (CPU generator) and their tensor scales."""
-    if not _ORACLE_W:
-        import oracle as O
-        import synth
-        for name, _, _ in DECODE_MATS:
-            w = synth.decode_weight(name).numpy()
-            _ORACLE_W[name] = (w, O.tensor_scale(w))
-    return _ORACLE_W
+PIN_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
 
 
-_ORACLE_X = {}
+def host_cores():
+    """(os.cpu_count(), cores this process may run on = nproc)."""
+    n_all = os.cpu_count() or 1
+    try:
+        n_aff = len(os.sched_getaffinity(0))
+    except Exception:
+        n_aff = n_all
+    return n_all, n_aff
 
 
-def _oracle_activation(M, K):
-    """The step's bf16 activations as fp32 on the host (drawn once; drawing
-    them is not the oracle's work)."""
-    import synth
-    if (M, K) not in _ORACLE_X:
-        _ORACLE_X[(M, K)] = synth.decode_activation(M, K).float().numpy()
-    return _ORACLE_X[(M, K)]
-
-
-def oracle_decode_sample(budget_s, rows_per_call=None):
-    """The oracle's W4A16 decode on a bounded sample: for each of the eight
-    calls, `rows_per_call` weight rows (quantised by the oracle with the full
-    tensor's scale) times the step's activations. With rows_per_call None the
-    sample is sized from a 16-row trial step so the step takes ~budget_s.
-    Returns (bytes, seconds, rows used)."""
+def prepare_oracle_weights(tmpdir):
+    """The decode weights on the host (CPU generator) as .npy files, and the
+    oracle's tensor scale of each (fp32, exact as a Python float)."""
     import numpy as np
 
     import oracle as O
-    mats = _oracle_weights()
-    if rows_per_call is None:
-        _, t_trial, _ = oracle_decode_sample(budget_s, 16)
-        rows_per_call = int(max(1, min(4096, 16 * budget_s / max(t_trial, 1e-3))))
-    rng = np.random.default_rng(0)
-    total_b, t_total = 0, 0.0
-    for M in DECODE_M:
-        for name, N, K in DECODE_MATS:
-            w, st = mats[name]
-            x = _oracle_activation(M, K)
-            r = np.sort(rng.choice(N, min(rows_per_call, N), replace=False))
-            t0 = time.perf_counter()
-            q = O.quantize(w[r], s_t=st)
-            O.gemm_w4a16(x, q)
-            t_total += time.perf_counter() - t0
-            total_b += len(r) * (K // 2 + K // 16) + 2 * M * K + 2 * M * len(r)
-    return total_b, t_total, rows_per_call
+    import synth
+    meta = {}
+    for name, _, _ in DECODE_MATS:
+        w = synth.decode_weight(name).numpy()
+        path = os.path.join(tmpdir, f"{name}.npy")
+        np.save(path, w)
+        meta[name] = {"path": path, "s_t": float(O.tensor_scale(w))}
+    return meta
+
+
+def cpu_leg(args):
+    """Child process: the oracle's W4A16 decode on a sample of weight rows per
+    call of the eight decode calls (rows quantised by the oracle with the full
+    tensor's scale, times the step's activations in fp64). --cpu-rows 0 sizes
+    the sample from a 16-row trial so one step takes ~--cpu-budget s. Prints
+    {bytes, seconds, rows, step_seconds} for the timed steps."""
+    import numpy as np
+
+    import oracle as O
+    import synth
+    meta = json.loads(args.cpu_meta)
+    mats = {name: (np.load(m["path"], mmap_mode="r"), np.float32(m["s_t"])) for name, m in meta.items()}
+    xs = {(M, K): synth.decode_activation(M, K).float().numpy() for M in DECODE_M for _, _, K in DECODE_MATS}
+    rng = np.random.default_rng(1000 + args.cpu_shard)
+
+    def step(rows):
+        b, t = 0, 0.0
+        for M in DECODE_M:
+            for name, N, K in DECODE_MATS:
+                w, st = mats[name]
+                r = np.sort(rng.choice(N, min(rows, N), replace=False))
+                wr = np.ascontiguousarray(w[r])       # rows read from the shared file: not the oracle's work
+                t0 = time.perf_counter()
+                q = O.quantize(wr, s_t=st)
+                O.gemm_w4a16(xs[(M, K)], q)
+                t += time.perf_counter() - t0
+                b += len(r) * (K // 2 + K // 16) + 2 * M * K + 2 * M * len(r)
+        return b, t
+
+    rows = args.cpu_rows
+    if rows <= 0:
+        _, t16 = step(16)
+        rows = int(max(1, min(4096, 16 * args.cpu_budget / max(t16, 1e-3))))
+    for _ in range(args.cpu_warmup):
+        step(rows)
+    tb, tt, per = 0, 0.0, []
+    for _ in range(args.cpu_steps):
+        b, t = step(rows)
+        tb, tt = tb + b, tt + t
+        per.append(t)
+    print(json.dumps({"bytes": tb, "seconds": tt, "rows": rows, "step_seconds": per}), flush=True)
+
+
+def cpu_children(meta, n, rows, steps, warmup, budget=0.0):
+    """Run n pinned oracle children at once (shards 0..n-1); their results."""
+    env = dict(os.environ, **PIN_ENV)
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-leg", "--cpu-meta", json.dumps(meta),
+           "--cpu-rows", str(rows), "--cpu-steps", str(steps), "--cpu-warmup", str(warmup), "--cpu-budget",
+           str(budget)]
+    procs = [subprocess.Popen(cmd + ["--cpu-shard", str(i)], stdout=subprocess.PIPE, env=env, text=True)
+             for i in range(n)]
+    outs = []
+    for p in procs:
+        o, _ = p.communicate(timeout=1200)
+        if p.returncode != 0:
+            raise RuntimeError(f"oracle child exited with {p.returncode}")
+        outs.append(json.loads(o.strip().splitlines()[-1]))
+    return outs
+
+
+def cpu_baseline(budget):
+    """The oracle on the host: one pinned core, then every available core."""
+    n_all, n_aff = host_cores()
+    with tempfile.TemporaryDirectory() as d:
+        meta = prepare_oracle_weights(d)
+        one = cpu_children(meta, 1, 0, 1, 0, budget)[0]
+        many = cpu_children(meta, n_aff, one["rows"], 1, 0)
+    v1 = one["bytes"] / one["seconds"] / 1e9
+    vall = sum(o["bytes"] for o in many) / max(o["seconds"] for o in many) / 1e9
+    return {"value": vall, "unit": "GB/s", "cores": n_aff, "kind": "oracle",
+            "sample": f"{one['rows']} weight rows per call of the 8 decode calls per process, oracle-quantised and "
+                      f"multiplied in fp64; {n_aff} single-threaded processes at once, each its own row sample "
+                      f"({max(o['seconds'] for o in many):.1f} s)",
+            "host_cores": n_all, "nproc": n_aff, "threads_per_process": 1, "pinning": PIN_ENV,
+            "single_core": {"value": v1, "unit": "GB/s", "cores": 1, "seconds": one["seconds"]}}
 
 
 # ------------------------------------------------------------------ main
@@ -542,7 +638,7 @@ def run_ours(args):
     tot_b, tot_t = 0.0, 0.0
     for M, name, N, K in dec.calls():
         g = capture(lambda M=M, name=name: [dec.call(M, name, r % REPLICAS) for r in range(12)])
-        t = time_graph(g, 5) / 12
+        t = time_graph(g, 20) / 12
         bts = decode_bytes(N, K, M)
         per_call[f"{name}_M{M}"] = {"us": t * 1e3, "gbs": bts / t / 1e6, "frac": bts / t / 1e6 / peaks["hbm_gbs"]}
         tot_b += bts
@@ -572,10 +668,7 @@ def run_ours(args):
                                    "reasons": clk["reasons"], "samples": clk["samples"]},
             "rows": rows}
     if rank == 0 and not args.no_cpu_baseline:
-        b_, t_, r_ = oracle_decode_sample(args.cpu_budget)
-        line["cpu_baseline"] = {"value": b_ / t_ / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{r_} weight rows per call of the 8 decode calls, oracle-quantised "
-                                          f"and multiplied in fp64 on the host ({t_:.1f} s)"}
+        line["cpu_baseline"] = cpu_baseline(args.cpu_budget)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -583,28 +676,30 @@ def run_ours(args):
 
 
 def run_reference(args):
+    """The oracle on the same metric and workload, on every available host
+    core (one pinned single-threaded process per core, each its own row
+    sample of every step), each step a bounded sample sized so the whole run
+    stays within a few minutes. Rank 0 only."""
     world, rank, _ = dist_info()
     if rank != 0:
         return
-    # each step a sample sized so the whole run stays within a few minutes
-    budget = min(8.0, 120.0 / max(1, args.steps + args.warmup + 1))
-    _, _, rows = oracle_decode_sample(budget)
-    for _ in range(args.warmup):
-        oracle_decode_sample(budget, rows)
-    tot_b, tot_t = 0, 0.0
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        b, t, _ = oracle_decode_sample(budget, rows)
-        tot_b += b
-        tot_t += t
-    wall = time.perf_counter() - t0
-    value = tot_b / tot_t / 1e9
+    n_all, n_aff = host_cores()
+    budget = min(8.0, 100.0 / max(1, args.steps + args.warmup))
+    with tempfile.TemporaryDirectory() as d:
+        meta = prepare_oracle_weights(d)
+        rows = cpu_children(meta, 1, 0, 1, 0, budget)[0]["rows"]
+        outs = cpu_children(meta, n_aff, rows, args.steps, args.warmup)
+    tot_b = sum(o["bytes"] for o in outs)
+    wall = max(o["seconds"] for o in outs)
+    value = tot_b / wall / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall * 1e3 / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded CPU RNG, distributions of the served layers)", "config": config_block(world),
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{rows} weight rows per call of the 8 decode calls per step"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": n_aff, "kind": "oracle",
+                             "sample": f"{rows} weight rows per call of the 8 decode calls per step and process, "
+                                       f"{n_aff} single-threaded processes at once",
+                             "host_cores": n_all, "nproc": n_aff, "pinning": PIN_ENV},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -662,14 +757,24 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--row-reps", type=int, default=10)
+    ap.add_argument("--row-reps", type=int, default=50, help="timed replays per row (median)")
     ap.add_argument("--no-rows", action="store_true", help="skip the non-headline rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work per core for cpu_baseline")
     ap.add_argument("--case", choices=["w4a4", "quantize", "draft", "moe"], default=None,
                     help="run one kernel family only (the profiling workloads)")
     ap.add_argument("--m", type=int, default=2048, help="rows / tokens for --case")
+    # the oracle child processes of the CPU legs
+    ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-meta", default="{}", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-rows", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-steps", type=int, default=1, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-warmup", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-shard", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_leg:
+        cpu_leg(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.case:

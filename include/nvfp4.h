@@ -138,6 +138,23 @@ int nvfp4_prepack_scales(const uint8_t* src, int64_t batch, int64_t rows, int64_
 int nvfp4_gemm_w4a16(const void* X, int64_t M, nvfp4_tensor_t W, void* Y,
                      void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
+/* Fused gate/up projection of a dense MLP with SiLU * mul in its epilogue:
+ * W stacks the gate rows [0, I) and the up rows [I, 2I) (W.rows = 2I), and
+ *   H[m][i] = bf16( silu(g) * u ),  g = sum_k X[m][k] W_hat[i][k],
+ *                                   u = sum_k X[m][k] W_hat[I + i][k]
+ * (g, u fp32-accumulated as in nvfp4_gemm_w4a16; silu(g) = g / (1 + e^-g)).
+ * The [M][2I] gate/up output never goes through memory: one round trip of
+ * the activations between two linears less, in the 4-bit-weight decoder
+ * layers of the pages (52.6% More Tokens..., comparison paragraph; the
+ * row order is the one the routed experts use, What 350+ Experiments...,
+ * section 1).
+ *   X  device bf16 [M][K];  W  NVFP4 [2I][K], batch 1, ROWMAJOR scales;
+ *   H  device bf16 [M][I];
+ *   workspace  >= nvfp4_workspace_size(NVFP4_OP_GEMM_W4A16, M, 2I, K) bytes.
+ * K must be a multiple of 256 and I a multiple of 64. */
+int nvfp4_gemm_w4a16_silu_mul(const void* X, int64_t M, nvfp4_tensor_t W, void* H,
+                              void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
 /* nvfp4_gemm_w4a16 without a workspace: the same computation and kernels, with
  * the converted activations and split-K partials kept in a fixed 8 MiB array of device
  * memory inside the library instead of caller memory. The pages have no
@@ -302,6 +319,16 @@ int nvfp4_read_device_status(int* out, nvfp4_stream_t stream);
  * nanoseconds, and records the outcome in the device status word. Used by the
  * tests to show that a wait that runs out returns an error instead of hanging. */
 int nvfp4_selftest_bounded_wait(int64_t limit_ns, nvfp4_stream_t stream);
+
+/* Measurement helper (no counterpart on the pages): the issue-rate ceiling of
+ * the block-scaled FP4 tensor cores on this GPU. Launches n_ctas CTAs (0 = one
+ * per SM), each issuing n_mma tcgen05.mma.kind::mxf4nvf4 instructions of
+ * 128 x 256 x 64 (2 * 128 * 256 * 64 flop each, the instruction of the W4A4
+ * kernels) into one tensor-memory accumulator from zero-filled shared memory,
+ * with no global memory traffic. The caller times the launch (e.g. with CUDA
+ * events on `stream`); flop / time is the rate the tensor pipe sustains.
+ * 1 <= n_mma <= 2^20, n_ctas >= 0. */
+int nvfp4_probe_fp4_mma_rate(int n_mma, int n_ctas, nvfp4_stream_t stream);
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 int nvfp4_version(void);

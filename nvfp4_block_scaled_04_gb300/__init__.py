@@ -27,7 +27,8 @@ EXPORTS = [
     "nvfp4_moe_route", "nvfp4_grouped_gemm", "nvfp4_gather_gemv_argmax", "nvfp4_gather_rows", "nvfp4_gemv_argmax",
     "nvfp4_scales_bytes", "nvfp4_workspace_size", "nvfp4_status_string",
     "nvfp4_read_device_status", "nvfp4_selftest_bounded_wait", "nvfp4_version",
-    "nvfp4_gemm_w4a16_noalloc", "nvfp4_verify_accept",
+    "nvfp4_gemm_w4a16_noalloc", "nvfp4_verify_accept", "nvfp4_probe_fp4_mma_rate",
+    "nvfp4_gemm_w4a16_silu_mul",
 ]
 _NON_INT = ("nvfp4_scales_bytes", "nvfp4_workspace_size", "nvfp4_status_string")
 
@@ -55,6 +56,7 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_gemm_w4a16.argtypes = [vp, i64, CTensor, vp, vp, sz, vp]
         L.nvfp4_gemm_w4a4.argtypes = [CTensor, CTensor, vp, vp, sz, vp]
         L.nvfp4_gemm_w4a16_noalloc.argtypes = [vp, i64, CTensor, vp, vp]
+        L.nvfp4_gemm_w4a16_silu_mul.argtypes = [vp, i64, CTensor, vp, vp, sz, vp]
         L.nvfp4_moe_route.argtypes = [vp, i64, i32, i32, vp, vp, vp]
         L.nvfp4_grouped_gemm.argtypes = [vp, i64, i32, vp, vp, CTensor, CTensor, vp, vp, sz, vp]
         L.nvfp4_gather_gemv_argmax.argtypes = [vp, i64, CTensor, vp, i64, vp, vp, vp, sz, vp]
@@ -69,6 +71,7 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_status_string.restype = ctypes.c_char_p
         L.nvfp4_read_device_status.argtypes = [ctypes.POINTER(ctypes.c_int), vp]
         L.nvfp4_selftest_bounded_wait.argtypes = [i64, vp]
+        L.nvfp4_probe_fp4_mma_rate.argtypes = [i32, i32, vp]
         L.nvfp4_version.argtypes = []
         for name in EXPORTS:
             if name not in _NON_INT:
@@ -182,6 +185,20 @@ def gemm_w4a16(x: torch.Tensor, w: QTensor, out: torch.Tensor | None = None,
     return y
 
 
+def gemm_w4a16_silu_mul(x: torch.Tensor, w: QTensor, out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """h = bf16(silu(X @ W_gate^T) * (X @ W_up^T)); W stacks gate rows [0, I)
+    and up rows [I, 2I). X bf16 [M][K] -> h bf16 [M][I]."""
+    _require_cuda(x)
+    M = x.shape[0]
+    h = out if out is not None else torch.empty(M, w.rows // 2, dtype=torch.bfloat16, device=x.device)
+    ws = workspace if workspace is not None else _workspace(workspace_size(OP_GEMM_W4A16, M, w.rows, w.K),
+                                                            x.device)
+    _check(lib().nvfp4_gemm_w4a16_silu_mul(_ptr(x), M, w.c(), _ptr(h), _ptr(ws), ws.numel(), _stream()),
+           "nvfp4_gemm_w4a16_silu_mul")
+    return h
+
+
 def gemm_w4a4(a: QTensor, w: QTensor, out: torch.Tensor | None = None,
               workspace: torch.Tensor | None = None) -> torch.Tensor:
     """Y = s_tA s_tW (A_q @ W_q^T) on the block-scaled FP4 tensor cores."""
@@ -279,6 +296,11 @@ def read_device_status() -> int:
     v = ctypes.c_int(0)
     _check(lib().nvfp4_read_device_status(ctypes.byref(v), _stream()), "nvfp4_read_device_status")
     return v.value
+
+
+def probe_fp4_mma_rate(n_mma: int, n_ctas: int = 0) -> None:
+    """Launch the FP4 tensor-core issue-rate probe on the current stream."""
+    _check(lib().nvfp4_probe_fp4_mma_rate(n_mma, n_ctas, _stream()), "nvfp4_probe_fp4_mma_rate")
 
 
 def selftest_bounded_wait(limit_ns: int) -> None:

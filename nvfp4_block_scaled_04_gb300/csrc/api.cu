@@ -133,6 +133,18 @@ int nvfp4_gemm_w4a16(const void* X, int64_t M, nvfp4_tensor_t W, void* Y, void* 
                            reinterpret_cast<cudaStream_t>(stream));
 }
 
+int nvfp4_gemm_w4a16_silu_mul(const void* X, int64_t M, nvfp4_tensor_t W, void* H, void* workspace,
+                              size_t workspace_bytes, nvfp4_stream_t stream) {
+  if (!X || !H || M < 0 || !tensor_ok(W) || W.batch != 1) return NVFP4_ERR_INVALID_ARG;
+  if (W.scale_layout != NVFP4_SCALES_ROWMAJOR) return NVFP4_ERR_INVALID_ARG;
+  if (W.K % 256 != 0 || W.rows % 128 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(X) || !aligned16(W.codes) || !aligned16(H)) return NVFP4_ERR_MISALIGNED;
+  if (M == 0 || W.rows == 0) return NVFP4_OK;
+  if (!workspace || workspace_bytes < w4a16_workspace_bytes(M, W.rows, W.K)) return NVFP4_ERR_WORKSPACE;
+  return launch_gemm_w4a16_silu_mul(static_cast<const uint16_t*>(X), M, W, static_cast<uint16_t*>(H), workspace,
+                                    reinterpret_cast<cudaStream_t>(stream));
+}
+
 int nvfp4_gemm_w4a4(nvfp4_tensor_t A, nvfp4_tensor_t W, void* Y, void* workspace, size_t workspace_bytes,
                     nvfp4_stream_t stream) {
   if (!Y || !tensor_ok(A) || !tensor_ok(W) || A.batch != 1 || W.batch != 1) return NVFP4_ERR_INVALID_ARG;
@@ -228,6 +240,12 @@ int nvfp4_verify_accept(const void* H, int64_t batch, int n_draft, nvfp4_tensor_
 int nvfp4_read_device_status(int* out, nvfp4_stream_t stream) {
   if (!out) return NVFP4_ERR_INVALID_ARG;
   return read_device_status(out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int nvfp4_probe_fp4_mma_rate(int n_mma, int n_ctas, nvfp4_stream_t stream) {
+  // at most 2^20 instructions (tens of milliseconds), far inside the kernel's 2 s bounded wait
+  if (n_mma < 1 || n_mma > (1 << 20) || n_ctas < 0) return NVFP4_ERR_INVALID_ARG;
+  return probe_fp4_mma_rate(n_mma, n_ctas, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int nvfp4_selftest_bounded_wait(int64_t limit_ns, nvfp4_stream_t stream) {

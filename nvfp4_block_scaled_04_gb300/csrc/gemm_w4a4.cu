@@ -718,6 +718,75 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(slot), "r"(32) : "memory");
 }
 
+// Issue-rate ceiling of the block-scaled FP4 tensor cores: one CTA per SM
+// issues `n_mma` tcgen05.mma.kind::mxf4nvf4 of 128 x 256 x 64 (the W4A4
+// kernels' instruction) back to back into one accumulator, operands from
+// shared memory (zeros) and block scales from tensor memory, no global
+// memory traffic; the tensor pipe is the only thing it can wait on. Timed by
+// the caller, it gives the FP4 rate this part reaches, for the W4A4 GEMM's
+// roofline beside the nominal figure. The completion wait is bounded.
+constexpr int PROBE_THREADS = 128;
+// more shared memory than two CTAs could share, so each SM holds one CTA and
+// no CTA waits for another's tensor memory
+constexpr int PROBE_SMEM = 120 * 1024;
+static_assert(A_BYTES + B_BYTES + 1024 + 64 <= PROBE_SMEM && 2 * PROBE_SMEM > 228 * 1024, "probe shared memory");
+__global__ void __launch_bounds__(PROBE_THREADS, 1) fp4_mma_rate_kernel(int n_mma) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bar = base + A_BYTES + B_BYTES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + A_BYTES + B_BYTES + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + A_BYTES + B_BYTES + 16);
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < (A_BYTES + B_BYTES) / 16; i += PROBE_THREADS)
+    reinterpret_cast<uint4*>(base_ptr)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the zeros are visible to the tensor pipe
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  {
+    // zero scale columns (E4M3 0 is a finite scale): each warp its lane quarter
+    uint32_t z[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) z[i] = 0u;
+    const uint32_t lane_cols = tmem + (static_cast<uint32_t>(warp * 32) << 16) + SF_TMEM_BASE;
+    tc_st_16cols(lane_cols, z);
+    tc_st_16cols(lane_cols + 16, z);
+    tc_st_16cols(lane_cols + 32, z);
+    tc_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+    const uint64_t adesc = smem_desc(base, 16, 1024, 2);
+    const uint64_t bdesc = smem_desc(base + A_BYTES, 16, 1024, 2);
+    for (int i = 0; i < n_mma; ++i)
+      tc_mma_mxf4nvf4(tmem, adesc, bdesc, IDESC, tmem + SF_TMEM_BASE, tmem + SF_TMEM_BASE + 16, i > 0 ? 1u : 0u);
+    tc_commit(bar);
+    mbar_wait_bounded(bar, 0, abort_flag, &g_device_status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
 // 2-D map over packed codes [rows][K/2] bytes, 128 x 128-byte boxes, 128B swizzle.
 int make_code_map(CUtensorMap* map, const uint8_t* codes, int64_t rows, int64_t K, int box_rows) {
   return make_tmap_2d_u8(map, codes, K / 2, rows, K / 2, 128, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -802,6 +871,14 @@ int read_device_status(int* out, cudaStream_t stream) {
   if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
   *out = v;
   return NVFP4_OK;
+}
+
+int probe_fp4_mma_rate(int n_mma, int n_ctas, cudaStream_t stream) {
+  int rc = ensure_smem(fp4_mma_rate_kernel, PROBE_SMEM);
+  if (rc != NVFP4_OK) return rc;
+  const int grid = n_ctas > 0 ? n_ctas : sm_count();
+  fp4_mma_rate_kernel<<<grid, PROBE_THREADS, PROBE_SMEM, stream>>>(n_mma);
+  return from_cuda(cudaGetLastError());
 }
 
 int selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream) {

@@ -228,6 +228,51 @@ int launch_gemm_w4a16(const uint16_t* X, int64_t M, const nvfp4_tensor_t& W, uin
   return launch_skinny_nt<SK_PLAIN>(nt, p, grid, stream);
 }
 
+// Dense gate/up projection with SiLU * mul fused: W [2I][K], gate rows
+// [0, I), up rows [I, 2I); tiles of 64 gate rows and the matching 64 up
+// rows, so each CTA holds both halves of its outputs; h = bf16(silu(g) * u).
+// The split along K, the warp layout and the reduction order are those of
+// the plain GEMV (the split is chosen from the 2I / 128 tiles of (N, K)).
+int launch_gemm_w4a16_silu_mul(const uint16_t* X, int64_t M, const nvfp4_tensor_t& W, uint16_t* H, void* ws,
+                               cudaStream_t stream) {
+  const int64_t K = W.K, N = W.rows, I = N / 2;
+  const DenseWs w = carve_dense(ws, M, N, K, false);
+  const int nt = static_cast<int>(ceil_div(M < GV_MCHUNK ? M : GV_MCHUNK, 8));
+  int rc = prep_dense(X, M, K, nt, w, stream);
+  if (rc != NVFP4_OK) return rc;
+  const int64_t row_tiles = I / 64, chunks = ceil_div(M, GV_MCHUNK);
+  CUtensorMap mc, ms;
+  rc = make_tmap_2d_u8(&mc, W.codes, K / 2, N, K / 2, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != NVFP4_OK) return rc;
+  rc = make_tmap_2d_u8(&ms, W.scales, K / 16, N, K / 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc != NVFP4_OK) return rc;
+  TmaSkinnyParams q{};
+  q.s_t = W.s_t;
+  q.K = K;
+  q.n_rows = N;
+  q.xfrag = w.xfrag;
+  q.pexp = w.pexp;
+  q.M = M;
+  q.split = tma_split(row_tiles, K / 256);
+  q.inter = I;
+  q.h_out = H;
+  q.status = device_status_ptr();
+  q.partials = w.partials;
+  q.counters = w.tile_counters;
+  dim3 grid(static_cast<unsigned>(q.split), static_cast<unsigned>(row_tiles), static_cast<unsigned>(chunks));
+  auto launch = [&](auto kernel, int smem) {
+    int r = ensure_smem(kernel, smem);
+    if (r != NVFP4_OK) return r;
+    return launch_ex(kernel, grid, dim3(GtWarps<2, 2>::THREADS), smem, 1, true, stream, mc, ms, q);
+  };
+  switch (nt) {
+    case 1: return launch(skinny_tma_kernel<1, SK_GATEUP_DENSE, 2, 2>, GtCfg<1>::SMEM);
+    case 2: return launch(skinny_tma_kernel<2, SK_GATEUP_DENSE, 2, 2>, GtCfg<2>::SMEM);
+    case 3: return launch(skinny_tma_kernel<3, SK_GATEUP_DENSE, 2, 2>, GtCfg<3>::SMEM);
+    default: return launch(skinny_tma_kernel<4, SK_GATEUP_DENSE, 2, 2>, GtCfg<4>::SMEM);
+  }
+}
+
 int launch_gather_rows(const nvfp4_tensor_t& W, const int32_t* idx, int64_t n_idx, uint8_t* codes_out,
                        uint8_t* scales_out, cudaStream_t stream) {
   constexpr int kWarps = 8;

@@ -223,7 +223,9 @@ NVFP4_DEV void gemv_mainloop(float (&acc)[NT][4], const uint8_t* cA, const uint8
   }
 }
 
-enum SkinnyMode { SK_PLAIN = 0, SK_ARGMAX = 1, SK_MOE_GATEUP = 2, SK_MOE_DOWN = 3 };
+// SK_GATEUP_DENSE: a dense gate/up projection W [2I][K] (gate rows [0, I),
+// up rows [I, 2I)) whose epilogue writes h = bf16(silu(g) * u) [M][I].
+enum SkinnyMode { SK_PLAIN = 0, SK_ARGMAX = 1, SK_MOE_GATEUP = 2, SK_MOE_DOWN = 3, SK_GATEUP_DENSE = 4 };
 
 struct SkinnyParams {
   // weights (row-major scales); batched tensors use global row ids

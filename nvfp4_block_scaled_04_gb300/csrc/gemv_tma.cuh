@@ -175,6 +175,8 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
     skinny_tma_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
                       const TmaSkinnyParams p) {
   constexpr bool GATHERED = MODE == SK_ARGMAX && GATHER;
+  // a tile of 64 gate rows and the matching 64 up rows, SiLU * mul fused
+  constexpr bool GATEUP = MODE == SK_MOE_GATEUP || MODE == SK_GATEUP_DENSE;
   using C = GtCfg<NT, GATHERED ? GT_SCALES_GATHERED : GT_SCALES>;
   pdl_launch_dependents();   // the next call's activation prep may queue up now
   constexpr int NCW = GtWarps<MT, KW>::CONSUMERS;
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int S = p.split;
-  const int s = (MODE == SK_PLAIN) ? static_cast<int>(blockIdx.x) : 0;
+  const int s = (MODE == SK_PLAIN || MODE == SK_GATEUP_DENSE) ? static_cast<int>(blockIdx.x) : 0;
   const int64_t n_it = p.K / GV_KIT;
   const int64_t n_st_total = (n_it + 1) / 2;
   const int st0 = static_cast<int>(n_st_total * s / S);
@@ -307,6 +309,9 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
       if (MODE == SK_MOE_GATEUP) {
         y_a = static_cast<int>(expert * p.rows_per_expert + row_tile * 64);
         y_b = static_cast<int>(expert * p.rows_per_expert + p.inter + row_tile * 64);
+      } else if (MODE == SK_GATEUP_DENSE) {
+        y_a = static_cast<int>(row_tile * 64);
+        y_b = static_cast<int>(p.inter + row_tile * 64);
       } else if (MODE == SK_MOE_DOWN) {
         y_a = static_cast<int>(expert * p.rows_per_expert + row_tile * GV_ROWS);
       } else {
@@ -327,14 +332,14 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
         // a weight byte read once per call is evicted from L2 first (measured:
         // decode step 183 -> 177 us, MoE layer at 256 tokens 173 -> 167 us);
         // routed experts with several token chunks re-read theirs
-        const bool once = MODE == SK_PLAIN || MODE == SK_ARGMAX || p.weights_once;
-        if (MODE == SK_MOE_GATEUP && once) {
+        const bool once = MODE == SK_PLAIN || MODE == SK_ARGMAX || MODE == SK_GATEUP_DENSE || p.weights_once;
+        if (GATEUP && once) {
           const uint64_t pol = l2_policy_evict_first();
           tma_load_2d_hint(stage, &map_codes, xc, y_a, full_bar(q), pol);
           tma_load_2d_hint(stage + GT_CODES / 2, &map_codes, xc, y_b, full_bar(q), pol);
           tma_load_2d_hint(stage + GT_CODES, &map_scales, xs, y_a, full_bar(q), pol);
           tma_load_2d_hint(stage + GT_CODES + GT_SCALES / 2, &map_scales, xs, y_b, full_bar(q), pol);
-        } else if (MODE == SK_MOE_GATEUP) {
+        } else if (GATEUP) {
           tma_load_2d(stage, &map_codes, xc, y_a, full_bar(q));
           tma_load_2d(stage + GT_CODES / 2, &map_codes, xc, y_b, full_bar(q));
           tma_load_2d(stage + GT_CODES, &map_scales, xs, y_a, full_bar(q));
@@ -420,7 +425,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
   const int64_t row_base = chunk * GV_MCHUNK;
   const float st = p.s_t[expert];
   if (S == 1) {
-    const int width = (MODE == SK_MOE_GATEUP) ? 64 : GV_ROWS;
+    const int width = GATEUP ? 64 : GV_ROWS;
     // ARGMAX: the loop runs warp-uniformly over whole rounds of NTHR, so each
     // round's keys can meet in a warp maximum before one shared atomic per
     // warp and token (a 128-byte row of outputs belongs to one token)
@@ -445,7 +450,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
             key = (static_cast<unsigned long long>(float_order_key(v * mul)) << 32) | (0xFFFFFFFFu - vid);
           }
           key_tok = tok;   // set for rows past the end too: the groups below follow the output index
-        } else if (MODE == SK_MOE_GATEUP) {
+        } else if (GATEUP) {
           const float gg = v * mul;
           const float uu = psum(tok, 64 + r) * mul;
           const float hh = gg / (1.0f + expf(-gg)) * uu;
@@ -502,7 +507,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
         }
       }
     }
-  } else if (MODE == SK_PLAIN) {
+  } else if (MODE == SK_PLAIN || MODE == SK_GATEUP_DENSE) {
     // split-K: partials to global memory, the last CTA of the tile reduces
     const int64_t tile = chunk * gridDim.y + row_tile;
     constexpr int P4 = GV_MCHUNK * GV_ROWS / 4;   // float4 groups of one split's partial
@@ -516,7 +521,38 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
     __syncthreads();
     if (tid == 0) *s_last = atomicAdd(&p.counters[tile], 1u) == static_cast<unsigned>(S - 1);
     __syncthreads();
-    if (*s_last) {
+    if (MODE == SK_GATEUP_DENSE && *s_last) {
+      // gate rows r .. r + 3 are float4 group tok * 32 + r / 4, the matching
+      // up rows group tok * 32 + 16 + r / 4; both summed in split order
+      __threadfence();
+      const float4* all = reinterpret_cast<const float4*>(p.partials) + tile * S * P4;
+      const int n4g = rows_in_chunk * 16;
+      for (int e = tid; e < n4g; e += NTHR) {
+        const int tok = e >> 4, gi = tok * 32 + (e & 15);
+        float4 xg[8], xu[8];
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq) {
+          xg[qq] = qq < S ? __ldcg(all + qq * P4 + gi) : make_float4(0.f, 0.f, 0.f, 0.f);
+          xu[qq] = qq < S ? __ldcg(all + qq * P4 + gi + 16) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float g4[4] = {0.f, 0.f, 0.f, 0.f}, u4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq)
+          if (qq < S) {
+            g4[0] += xg[qq].x; g4[1] += xg[qq].y; g4[2] += xg[qq].z; g4[3] += xg[qq].w;
+            u4[0] += xu[qq].x; u4[1] += xu[qq].y; u4[2] += xu[qq].z; u4[3] += xu[qq].w;
+          }
+        const float mul = ldexpf(st, pexp_s[tok]);
+        float h4[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float gg = g4[c] * mul, uu = u4[c] * mul;
+          h4[c] = gg / (1.0f + expf(-gg)) * uu;
+        }
+        *reinterpret_cast<uint2*>(p.h_out + (row_base + tok) * p.inter + row_tile * 64 + (e & 15) * 4) =
+            make_uint2(f32x2_to_bf16x2(h4[0], h4[1]), f32x2_to_bf16x2(h4[2], h4[3]));
+      }
+    } else if (*s_last) {
       __threadfence();
       const float4* all = reinterpret_cast<const float4*>(p.partials) + tile * S * P4;
       // two groups per thread per round, all S (<= 8) partials of both requested before any

@@ -81,6 +81,8 @@ size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K);
 size_t argmax_workspace_bytes(int64_t M, int64_t K);
 int launch_gemm_w4a16(const uint16_t* X, int64_t M, const nvfp4_tensor_t& W, uint16_t* Y, void* ws,
                       cudaStream_t stream);
+int launch_gemm_w4a16_silu_mul(const uint16_t* X, int64_t M, const nvfp4_tensor_t& W, uint16_t* H, void* ws,
+                               cudaStream_t stream);
 int launch_gather_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, const int32_t* idx,
                          int64_t n_idx, int32_t* out_ids, float* out_logit, void* ws, cudaStream_t stream);
 int launch_gather_rows(const nvfp4_tensor_t& W, const int32_t* idx, int64_t n_idx, uint8_t* codes_out,
@@ -103,5 +105,6 @@ int launch_gemm_w4a4(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t*
                      cudaStream_t stream);
 int read_device_status(int* out, cudaStream_t stream);
 int selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream);
+int probe_fp4_mma_rate(int n_mma, int n_ctas, cudaStream_t stream);
 
 }  // namespace nvfp4

@@ -35,3 +35,21 @@ def test_errors_are_reported_not_raised_on_device():
     x = torch.zeros(4, 40, device=DEV)
     with pytest.raises(RuntimeError, match="unsupported shape"):
         m.quantize(x)
+
+
+def test_fp4_mma_rate_probe_runs_and_reports_ok():
+    """The FP4 tensor-pipe ceiling probe finishes (its bounded wait does not
+    give up) and its rate is a plausible fraction of the nominal dense FP4
+    figure: above 1 PFLOP/s, below 20."""
+    m = nv()
+    m.read_device_status()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    m.probe_fp4_mma_rate(100)   # warm-up
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    m.probe_fp4_mma_rate(20000)
+    b.record()
+    torch.cuda.synchronize()
+    assert m.read_device_status() == m.OK
+    pflops = sms * 20000 * 2.0 * 128 * 256 * 64 / (a.elapsed_time(b) * 1e-3) / 1e15
+    assert 1.0 < pflops < 20.0, pflops

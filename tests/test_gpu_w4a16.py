@@ -143,3 +143,53 @@ def test_token_bits_do_not_depend_on_batch(N, K):
         rows.append(m.gemm_w4a16(x, qw)[pos].clone())
     for M, r in zip((8, 17, 32, 33, 70), rows[1:]):
         assert torch.equal(r.view(torch.int16), rows[0].view(torch.int16)), M
+
+
+def silu_mul_ref(x_bf16, wq_gate, wq_up):
+    """Oracle: h = bf16(silu(g) * u) from fp64 g, u (reading R7 on a dense layer)."""
+    x = x_bf16.float().numpy()
+    return O.bf16_round(O.silu(O.gemm_w4a16(x, wq_gate)) * O.gemm_w4a16(x, wq_up))
+
+
+@pytest.mark.parametrize("M", [1, 5, 32, 40])
+@pytest.mark.parametrize("I,K", [(128, 4096), (256, 256), (192, 1024)])
+def test_silu_mul_fused_gate_up(M, I, K):
+    """(128, 4096) splits K across CTAs; (256, 256) does not; M = 40 spans two token chunks."""
+    m = nv()
+    w = synth.normal_f32((2 * I, K), 0.02, seed=I + K)
+    x = synth.normal_bf16((M, K), seed=M + 7)
+    h = np_f64(m.gemm_w4a16_silu_mul(x.to(DEV), m.quantize(w.to(DEV))))
+    st = O.tensor_scale(w.numpy())
+    ref = silu_mul_ref(x, O.quantize(w.numpy()[:I], s_t=st), O.quantize(w.numpy()[I:], s_t=st))
+    assert h.shape == (M, I)
+    assert O.rel_fro(h, ref) <= TOL
+
+
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_silu_mul_27b_gate_up_sampled(M):
+    """The 27B gate/up (5120 -> 2 x 17408) with SiLU * mul fused: 256 sampled
+    intermediate columns against the oracle (gate row i and up row I + i,
+    quantised with the whole tensor's scale)."""
+    m = nv()
+    wt, qw, st = _decode_weight("gate_up")
+    w = wt.numpy()
+    I = w.shape[0] // 2
+    x = synth.decode_activation(M, w.shape[1])
+    h = np_f64(m.gemm_w4a16_silu_mul(x.to(DEV), qw))
+    cols = np.sort(np.random.default_rng(M).choice(I, 256, replace=False))
+    ref = silu_mul_ref(x, O.quantize(w[cols], s_t=st), O.quantize(w[I + cols], s_t=st))
+    assert O.rel_fro(h[:, cols], ref) <= TOL
+
+
+def test_silu_mul_rows_do_not_depend_on_batch():
+    m = nv()
+    I, K = 256, 4096
+    qw = m.quantize(synth.normal_f32((2 * I, K), 0.02, seed=77).to(DEV))
+    tok = synth.normal_bf16((1, K), seed=78).to(DEV)
+    rows = []
+    for M in (1, 9, 32, 33):
+        x = synth.normal_bf16((M, K), seed=M + 200).to(DEV)
+        x[M - 1] = tok[0]
+        rows.append(m.gemm_w4a16_silu_mul(x, qw)[M - 1].clone())
+    for r in rows[1:]:
+        assert torch.equal(r.view(torch.int16), rows[0].view(torch.int16))
