@@ -340,6 +340,33 @@ def e2e_graph(dec):
     return capture(fn), h2d, d2h
 
 
+def measure_silu_mul(nv, peaks, reps):
+    """The 27B gate/up with SiLU * mul fused (h [M][17408] written once)
+    against the plain gate/up GEMV (y [M][34816] written, then read back by a
+    separate SiLU * mul): per call, weights rotated over six replicas."""
+    import torch
+    N, K = 34816, 5120
+    wf = gpu_normal((N, K), 0.02, seed=100)
+    q = nv.quantize(wf)
+    del wf
+    reps_w = [q] + [nv.QTensor(q.codes.clone(), q.scales.clone(), q.s_t.clone(), N, K) for _ in range(REPLICAS - 1)]
+    res = {}
+    for M in DECODE_M:
+        x = gpu_normal((M, K), 1.0, seed=300 + M, dtype=torch.bfloat16)
+        h = torch.empty(M, N // 2, dtype=torch.bfloat16, device="cuda")
+        y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(nv.workspace_size(nv.OP_GEMM_W4A16, M, N, K), dtype=torch.uint8, device="cuda")
+        gf = capture(lambda: [nv.gemm_w4a16_silu_mul(x, reps_w[r % REPLICAS], out=h, workspace=ws)
+                              for r in range(12)])
+        gp = capture(lambda: [nv.gemm_w4a16(x, reps_w[r % REPLICAS], out=y, workspace=ws) for r in range(12)])
+        tf, tp = time_graph(gf, 20) / 12, time_graph(gp, 20) / 12
+        b = decode_bytes(N, K, M) - 2 * M * N + 2 * M * (N // 2)
+        res[f"M{M}"] = {"us_fused": tf * 1e3, "us_plain_gemv": tp * 1e3, "gbs_fused": b / tf / 1e6,
+                        "frac_hbm_fused": b / tf / 1e6 / peaks["hbm_gbs"],
+                        "bytes_saved_vs_unfused": 4 * M * N}
+    return res
+
+
 # --------------------------------------------------------- the other rows
 
 def measure_rows(nv, peaks, reps):
@@ -390,7 +417,25 @@ def measure_rows(nv, peaks, reps):
     qbytes = M * K * 2 + M * K // 2 + M * K // 16
     out["quantize_activations"] = {"shape": [M, K], "ms": tq, "gbs": qbytes / tq / 1e6,
                                    "frac_hbm": qbytes / tq / 1e6 / peaks["hbm_gbs"]}
-    del a, qa, qw, y, g, g2, gq
+
+    # the same GEMM handing its output on as NVFP4 (the next W4A4 layer's
+    # input): fused epilogue with a given tensor scale, the dynamic two-pass
+    # form, and the unfused bf16 GEMM + quantiser it replaces
+    st_out = torch.tensor([0.05], device="cuda")
+    wsq = torch.empty(nv.workspace_size(nv.OP_GEMM_W4A4_QUANT, M, N, K), dtype=torch.uint8, device="cuda")
+    codes_o = torch.empty(M, N // 2, dtype=torch.uint8, device="cuda")
+    gf = capture(lambda: nv.gemm_w4a4_quant(qa, qw, s_t=st_out, workspace=wsq))
+    tf = time_graph(gf, reps)
+    gd = capture(lambda: nv.gemm_w4a4_quant(qa, qw, y=y, workspace=wsq))
+    td = time_graph(gd, reps)
+    qws2 = torch.empty(nv.workspace_size(nv.OP_QUANTIZE, M, 0, N), dtype=torch.uint8, device="cuda")
+    gu = capture(lambda: (nv.gemm_w4a4(qa, qw, out=y), nv.quantize(y, scale_layout=nv.SCALES_MMA, workspace=qws2)))
+    tu = time_graph(gu, reps)
+    out["w4a4_to_nvfp4"] = {
+        "shape": [M, N, K], "ms_fused_given_scale": tf, "ms_dynamic_scale_two_pass": td, "ms_unfused": tu,
+        "tflops_fused": flops / tf / 1e9, "bf16_round_trip_bytes_saved_fused": 2 * M * N * 2,
+        "note": "unfused = bf16 GEMM output written, then read twice by the quantiser (amax + encode)"}
+    del a, qa, qw, y, g, g2, gq, gf, gd, gu, codes_o
     torch.cuda.empty_cache()
 
     # masked draft head: 248,320 x 5120, 32,768-id mask, M in {1, 4, 8}
@@ -652,6 +697,8 @@ def run_ours(args):
            "d2h_bytes_per_step": d2h, "ms_per_step": te}
 
     rows = measure_rows(nv, peaks, reps=args.row_reps) if not args.no_rows else {}
+    if not args.no_rows:
+        rows["gate_up_silu_mul_fused"] = measure_silu_mul(nv, peaks, args.row_reps)
 
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",

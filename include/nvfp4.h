@@ -93,6 +93,7 @@ typedef struct nvfp4_tensor {
 #define NVFP4_OP_GEMM_W4A4       2
 #define NVFP4_OP_GROUPED_GEMM    3
 #define NVFP4_OP_GATHER_ARGMAX   4
+#define NVFP4_OP_GEMM_W4A4_QUANT 5
 
 /* ---- entry points ----------------------------------------------------------- */
 
@@ -189,6 +190,28 @@ int nvfp4_gemm_w4a16_noalloc(const void* X, int64_t M, nvfp4_tensor_t W, void* Y
  * K must be a multiple of 64 and N a multiple of 8; M >= 1 arbitrary. */
 int nvfp4_gemm_w4a4(nvfp4_tensor_t A, nvfp4_tensor_t W, void* Y,
                     void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* W4A4 linear whose output goes on as NVFP4, the input of the next W4A4
+ * layer: W4A4 end to end, with no bf16 activation between the two linears
+ * making a round trip through memory in the fused case (52.6% More
+ * Tokens..., comparison paragraph). The output is the quantisation (the
+ * rules of nvfp4_quantize, MMA-layout scales) of the bf16 output
+ * Y = bf16(s_tA * s_tW * sum_k a * w) that nvfp4_gemm_w4a4 would write:
+ *   NVFP4_ST_GIVEN    *s_t is the output's tensor scale (a static,
+ *                     calibrated one): one fused kernel, whose epilogue
+ *                     quantises each row's 16-column blocks; Y is not written
+ *                     and may be NULL.
+ *   NVFP4_ST_COMPUTE  s_t = amax(|Y|) / 2688 (1 if Y is all zero), written to
+ *                     *s_t: a tensor-wide amax is needed before any block can
+ *                     be encoded, so the GEMM writes Y (bf16, caller buffer
+ *                     [M][N]) and folds its amax on the fly, and a second
+ *                     kernel encodes Y without another amax pass.
+ *   A, W       as for nvfp4_gemm_w4a4; N (W.rows) a multiple of 64
+ *   codes      device out [M][N/2];  scales device out, nvfp4_scales_bytes(M, N,
+ *              NVFP4_SCALES_MMA) bytes (padding bytes written as zero)
+ *   workspace  >= nvfp4_workspace_size(NVFP4_OP_GEMM_W4A4_QUANT, M, N, K). */
+int nvfp4_gemm_w4a4_quant(nvfp4_tensor_t A, nvfp4_tensor_t W, uint8_t* codes, uint8_t* scales, float* s_t,
+                          int s_t_mode, void* Y, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /* Top-k routing of a MoE layer: p = softmax(logits[t]) (fp32), the k experts
  * with the largest p (ties to the lower expert id), weights = those p (not
@@ -301,7 +324,8 @@ size_t nvfp4_scales_bytes(int64_t rows, int64_t K, int scale_layout);
  *   GEMM_W4A16:    (M, N, K, -, -)
  *   GEMM_W4A4:     (M, N, K, -, -)   (worst case: both operands ROWMAJOR)
  *   GROUPED_GEMM:  (T, H, I, E, topk)
- *   GATHER_ARGMAX: (M, n_idx, K, -, -) */
+ *   GATHER_ARGMAX: (M, n_idx, K, -, -)
+ *   GEMM_W4A4_QUANT: (M, N, K, -, -) */
 size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t c, int64_t e, int64_t topk);
 
 /* Human-readable name of a status code (static storage). */

@@ -20,7 +20,7 @@ ERR_INVALID_ARG, ERR_TIMEOUT = -1, -6
 DTYPE_F32, DTYPE_BF16 = 0, 1
 ST_COMPUTE, ST_GIVEN = 0, 1
 SCALES_ROWMAJOR, SCALES_MMA = 0, 1
-OP_QUANTIZE, OP_GEMM_W4A16, OP_GEMM_W4A4, OP_GROUPED_GEMM, OP_GATHER_ARGMAX = range(5)
+OP_QUANTIZE, OP_GEMM_W4A16, OP_GEMM_W4A4, OP_GROUPED_GEMM, OP_GATHER_ARGMAX, OP_GEMM_W4A4_QUANT = range(6)
 
 EXPORTS = [
     "nvfp4_quantize", "nvfp4_prepack_scales", "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4",
@@ -28,7 +28,7 @@ EXPORTS = [
     "nvfp4_scales_bytes", "nvfp4_workspace_size", "nvfp4_status_string",
     "nvfp4_read_device_status", "nvfp4_selftest_bounded_wait", "nvfp4_version",
     "nvfp4_gemm_w4a16_noalloc", "nvfp4_verify_accept", "nvfp4_probe_fp4_mma_rate",
-    "nvfp4_gemm_w4a16_silu_mul",
+    "nvfp4_gemm_w4a16_silu_mul", "nvfp4_gemm_w4a4_quant",
 ]
 _NON_INT = ("nvfp4_scales_bytes", "nvfp4_workspace_size", "nvfp4_status_string")
 
@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_prepack_scales.argtypes = [vp, i64, i64, i64, vp, vp]
         L.nvfp4_gemm_w4a16.argtypes = [vp, i64, CTensor, vp, vp, sz, vp]
         L.nvfp4_gemm_w4a4.argtypes = [CTensor, CTensor, vp, vp, sz, vp]
+        L.nvfp4_gemm_w4a4_quant.argtypes = [CTensor, CTensor, vp, vp, vp, i32, vp, vp, sz, vp]
         L.nvfp4_gemm_w4a16_noalloc.argtypes = [vp, i64, CTensor, vp, vp]
         L.nvfp4_gemm_w4a16_silu_mul.argtypes = [vp, i64, CTensor, vp, vp, sz, vp]
         L.nvfp4_moe_route.argtypes = [vp, i64, i32, i32, vp, vp, vp]
@@ -208,6 +209,29 @@ def gemm_w4a4(a: QTensor, w: QTensor, out: torch.Tensor | None = None,
                                                             a.codes.device)
     _check(lib().nvfp4_gemm_w4a4(a.c(), w.c(), _ptr(y), _ptr(ws), ws.numel(), _stream()), "nvfp4_gemm_w4a4")
     return y
+
+
+def gemm_w4a4_quant(a: QTensor, w: QTensor, s_t: torch.Tensor | None = None, y: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None) -> QTensor:
+    """The W4A4 output as NVFP4 (MMA-layout scales), the next W4A4 layer's
+    input. s_t given -> fused epilogue with that tensor scale; None -> the
+    dynamic scale amax / 2688 (the bf16 output is written to `y` on the way)."""
+    _require_cuda(a.codes)
+    M, N = a.rows, w.rows
+    dev = a.codes.device
+    codes = torch.empty(M, N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(max(scales_bytes(M, N, SCALES_MMA), 1), dtype=torch.uint8, device=dev)
+    if s_t is None:
+        st = torch.empty(1, dtype=torch.float32, device=dev)
+        mode = ST_COMPUTE
+        y = y if y is not None else torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    else:
+        st = s_t.to(device=dev, dtype=torch.float32).reshape(1).contiguous()
+        mode = ST_GIVEN
+    ws = workspace if workspace is not None else _workspace(workspace_size(OP_GEMM_W4A4_QUANT, M, N, a.K), dev)
+    _check(lib().nvfp4_gemm_w4a4_quant(a.c(), w.c(), _ptr(codes), _ptr(scales), _ptr(st), mode, _ptr(y), _ptr(ws),
+                                       ws.numel(), _stream()), "nvfp4_gemm_w4a4_quant")
+    return QTensor(codes, scales, st, M, N, 1, SCALES_MMA)
 
 
 def moe_route(logits: torch.Tensor, topk: int):

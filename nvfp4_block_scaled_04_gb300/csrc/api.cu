@@ -92,6 +92,7 @@ size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t c, int64_t e, 
     case NVFP4_OP_QUANTIZE: return quantize_workspace_bytes();
     case NVFP4_OP_GEMM_W4A16: return a > 0 && c > 0 ? w4a16_workspace_bytes(a, b, c) : 0;
     case NVFP4_OP_GEMM_W4A4: return w4a4_workspace_bytes(a, b, c);
+    case NVFP4_OP_GEMM_W4A4_QUANT: return w4a4_quant_workspace_bytes(a, b, c);
     case NVFP4_OP_GROUPED_GEMM: return grouped_workspace_bytes(a, b, c, e, topk);
     case NVFP4_OP_GATHER_ARGMAX: return a > 0 && c > 0 ? argmax_workspace_bytes(a, c) : 0;
     default: return 0;
@@ -159,6 +160,23 @@ int nvfp4_gemm_w4a4(nvfp4_tensor_t A, nvfp4_tensor_t W, void* Y, void* workspace
   if (relayout && (!workspace || workspace_bytes < w4a4_workspace_bytes(A.rows, W.rows, A.K)))
     return NVFP4_ERR_WORKSPACE;
   return launch_gemm_w4a4(A, W, static_cast<uint16_t*>(Y), workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int nvfp4_gemm_w4a4_quant(nvfp4_tensor_t A, nvfp4_tensor_t W, uint8_t* codes, uint8_t* scales, float* s_t,
+                          int s_t_mode, void* Y, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+  if (!codes || !scales || !s_t || !tensor_ok(A) || !tensor_ok(W) || A.batch != 1 || W.batch != 1)
+    return NVFP4_ERR_INVALID_ARG;
+  if (s_t_mode != NVFP4_ST_COMPUTE && s_t_mode != NVFP4_ST_GIVEN) return NVFP4_ERR_INVALID_ARG;
+  if (s_t_mode == NVFP4_ST_COMPUTE && !Y) return NVFP4_ERR_INVALID_ARG;
+  if (A.K != W.K) return NVFP4_ERR_INVALID_ARG;
+  if (A.K % 64 != 0 || W.rows % 64 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(A.codes) || !aligned16(W.codes) || !aligned16(A.scales) || !aligned16(W.scales) ||
+      !aligned16(codes) || !aligned16(scales) || (Y && !aligned16(Y)))
+    return NVFP4_ERR_MISALIGNED;
+  if (A.rows == 0 || W.rows == 0) return NVFP4_OK;
+  if (!workspace || workspace_bytes < w4a4_quant_workspace_bytes(A.rows, W.rows, A.K)) return NVFP4_ERR_WORKSPACE;
+  return launch_gemm_w4a4_quant(A, W, codes, scales, s_t, s_t_mode, static_cast<uint16_t*>(Y), workspace,
+                                reinterpret_cast<cudaStream_t>(stream));
 }
 
 int nvfp4_moe_route(const float* logits, int64_t T, int E, int topk, int32_t* ids, float* weights,

@@ -26,6 +26,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "quant_core.cuh"
 #include "tc_util.cuh"
 #include "tcgen05.cuh"
 
@@ -92,7 +93,85 @@ struct W4A4Params {
   uint16_t* Y;
   int M, N, K;
   int m_tiles, n_tiles;
+  // EPI_QUANT: the output as NVFP4 with tensor scale *q_st (N % 64 == 0)
+  uint8_t* q_codes;          // [M][N/2]
+  uint8_t* q_scales;         // MMA layout: rows padded to 128, N/16 scale columns
+  const float* q_st;
+  // EPI_AMAX: max |bf16 output| as fp32 bits (atomicMax; zero on entry)
+  unsigned int* amax_bits;
 };
+
+// What an epilogue thread does with its row's 128 bf16 outputs (packed in
+// pairs: packed[i] holds columns 2i, 2i + 1):
+//   EPI_BF16   store them (Y)
+//   EPI_QUANT  quantise them to NVFP4 with the given tensor scale (the same
+//              per-16 block step as the quantiser, on the bf16 values the
+//              unfused layer would hand on) and store codes and MMA-layout
+//              scales; Y is not written
+//   EPI_AMAX   store them and fold their largest magnitude into amax_bits,
+//              for a quantiser pass with a dynamic tensor scale that then
+//              skips its own amax pass
+constexpr int EPI_BF16 = 0, EPI_QUANT = 1, EPI_AMAX = 2;
+
+// EPI_QUANT for one row: `tile_ok` says the row's 128-row tile exists in the
+// padded scale layout; rows in it past M get their (zero) scales but no codes.
+NVFP4_DEV void epi_quant_row(const W4A4Params& p, const uint32_t (&packed)[64], int row, int col0, bool tile_ok) {
+  if (!tile_ok || col0 >= p.N) return;
+  const float st = *p.q_st;
+  const float d = __fmul_rn(st, 6.0f);
+  const int nblk = min(8, (p.N - col0) / 16);   // 4 or 8 (N % 64 == 0)
+  uint32_t scw[2] = {0u, 0u};
+  uint4 cw[4];
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    float v[16];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t w = packed[8 * b + e];
+      v[2 * e] = __uint_as_float(w << 16);
+      v[2 * e + 1] = __uint_as_float(w & 0xFFFF0000u);
+    }
+    uint2 c;
+    const uint32_t sc = quant_block16(v, st, d, c);
+    scw[b >> 2] |= sc << (8 * (b & 3));
+    if (b & 1) {
+      cw[b >> 1].z = c.x;
+      cw[b >> 1].w = c.y;
+    } else {
+      cw[b >> 1].x = c.x;
+      cw[b >> 1].y = c.y;
+    }
+  }
+  if (row < p.M) {
+    uint4* dst = reinterpret_cast<uint4*>(p.q_codes + static_cast<int64_t>(row) * (p.N / 2) + col0 / 2);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (2 * q < nblk) dst[q] = cw[q];
+  }
+  // scale byte (row, c) of the MMA layout with N/16 columns (a multiple of 4):
+  // ((row / 128) * (N / 64) + c / 4) * 512 + (row % 32) * 16 + ((row / 32) % 4) * 4 + c % 4
+  const int c0 = col0 / 16;
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+    if (4 * g < nblk) {
+      const int c = c0 + 4 * g;
+      const int64_t off = (static_cast<int64_t>(row >> 7) * (p.N / 64) + (c >> 2)) * 512 + (row & 31) * 16 +
+                          ((row >> 5) & 3) * 4;
+      *reinterpret_cast<uint32_t*>(p.q_scales + off) = scw[g];
+    }
+}
+
+// EPI_AMAX: the warp's largest output magnitude into amax_bits.
+NVFP4_DEV void epi_amax(const W4A4Params& p, const uint32_t (&packed)[64], bool valid) {
+  uint32_t m = 0u;
+  if (valid) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) m = max(m, max(packed[i] & 0x7FFFu, (packed[i] >> 16) & 0x7FFFu));
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  // bf16 magnitude bits order like the values; as fp32 bits they are m << 16
+  if ((threadIdx.x & 31) == 0 && m != 0u) atomicMax(p.amax_bits, m << 16);
+}
 
 // tile index -> (m_tile, n_tile): bands of BAND m-tiles sweep all n-tiles,
 // m fastest, so the CTAs working at one time share A and W tiles in L2
@@ -117,6 +196,7 @@ NVFP4_DEV void tile_coords(int tile, const W4A4Params& p, int& m_tile, int& n_ti
 //               memory into that stage's tensor-memory scale columns
 // A warp may touch only the tensor-memory lane quarter warp % 4; every branch
 // that ends in a .sync.aligned tcgen05 instruction is taken warp-uniformly.
+template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_w4a4_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                      const W4A4Params p) {
@@ -266,6 +346,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(acce_bar);
       const int row = m_tile * BM + quarter * 32 + lane;
       const int col0 = n_tile * BN + half * 128;
+      if (EPI == EPI_QUANT) {
+        epi_quant_row(p, packed, row, col0, true);
+        continue;
+      }
+      if (EPI == EPI_AMAX) epi_amax(p, packed, row < p.M && col0 < p.N);
       if (row < p.M && col0 < p.N) {
         uint16_t* dst = p.Y + static_cast<int64_t>(row) * p.N + col0;
         const int nq = (p.N - col0) >= 128 ? 16 : (p.N - col0) / 8;   // 16-byte pieces in range
@@ -452,6 +537,7 @@ NVFP4_DEV void pair_coords(int tile, int m_pairs, int n_tiles, int& m_pair, int&
 
 // Warp roles as in gemm_w4a4_kernel, in both CTAs; in the odd CTA warp 1 only
 // takes part in the tensor-memory allocation.
+template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                           const __grid_constant__ CUtensorMap map_y, const W4A4Params p) {
@@ -495,7 +581,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_a) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&map_b) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_y) : "memory");
+    if (EPI != EPI_QUANT) asm volatile("prefetch.tensormap [%0];" ::"l"(&map_y) : "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -601,10 +687,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acce_bar, 0);
-      // two 64-column boxes through this warp's staging buffer (128B swizzle:
-      // 16-byte chunk c of row r at r * 128 + (c ^ (r % 8)) * 16)
       const int row0 = (2 * m_pair + static_cast<int>(rank)) * BM + quarter * 32;
       const int col0 = n_tile * BN + half * 128;
+      if (EPI == EPI_QUANT) {
+        epi_quant_row(p, packed, row0 + lane, col0, 2 * m_pair + static_cast<int>(rank) < p.m_tiles);
+        continue;
+      }
+      if (EPI == EPI_AMAX) epi_amax(p, packed, 2 * m_pair + static_cast<int>(rank) < p.m_tiles && row0 + lane < p.M);
+      // two 64-column boxes through this warp's staging buffer (128B swizzle:
+      // 16-byte chunk c of row r at r * 128 + (c ^ (r % 8)) * 16)
       const uint32_t stage_out = out_base + static_cast<uint32_t>(warp - EPI_WARP0) * P_OUT_BYTES;
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
@@ -802,8 +893,11 @@ size_t w4a4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
          align_up(static_cast<size_t>(mma_scale_rows(N) * mma_scale_cols(K)));
 }
 
-int launch_gemm_w4a4(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t* Y, void* ws,
-                     cudaStream_t stream) {
+namespace {
+
+template <int EPI>
+int launch_w4a4_epi(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t* Y, void* ws, cudaStream_t stream,
+                    uint8_t* q_codes, uint8_t* q_scales, const float* q_st, unsigned int* amax_bits) {
   const int64_t M = A.rows, N = W.rows, K = A.K;
   if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   const uint8_t* sfa = A.scales;
@@ -828,9 +922,13 @@ int launch_gemm_w4a4(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t*
   rc = make_code_map(&map_b, W.codes, N, K, BN);
   if (rc != NVFP4_OK) return rc;
 
-  rc = ensure_smem(gemm_w4a4_kernel, SMEM_BYTES);
+  rc = ensure_smem(gemm_w4a4_kernel<EPI>, SMEM_BYTES);
   if (rc != NVFP4_OK) return rc;
   W4A4Params p{};
+  p.q_codes = q_codes;
+  p.q_scales = q_scales;
+  p.q_st = q_st;
+  p.amax_bits = amax_bits;
   p.sfa = sfa;
   p.sfb = sfb;
   p.st_a = A.s_t;
@@ -845,22 +943,48 @@ int launch_gemm_w4a4(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t*
     // CTA pairs on 256 x 256 tiles: W tiles come in 128-row halves
     rc = make_code_map(&map_b, W.codes, N, K, 128);
     if (rc != NVFP4_OK) return rc;
-    rc = ensure_smem(gemm_w4a4_pair_kernel, P_SMEM_BYTES);
+    rc = ensure_smem(gemm_w4a4_pair_kernel<EPI>, P_SMEM_BYTES);
     if (rc != NVFP4_OK) return rc;
-    // bf16 Y [M][N]: stores of 64 columns x 32 rows (N % 8 == 0 keeps the row stride 16-byte aligned)
-    CUtensorMap map_y;
-    rc = make_tmap_2d_u16(&map_y, Y, N, M, N * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (rc != NVFP4_OK) return rc;
+    // bf16 Y [M][N]: stores of 64 columns x 32 rows (N % 8 == 0 keeps the row stride 16-byte aligned);
+    // the quantising epilogue writes no Y and never touches the map
+    CUtensorMap map_y{};
+    if (EPI != EPI_QUANT) {
+      rc = make_tmap_2d_u16(&map_y, Y, N, M, N * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc != NVFP4_OK) return rc;
+    }
     const int64_t pair_tiles = ceil_div(p.m_tiles, 2) * p.n_tiles;
     const int64_t max_pairs = sm_count() / 2;
     const unsigned grid = static_cast<unsigned>(2 * (pair_tiles < max_pairs ? pair_tiles : max_pairs));
-    return launch_ex(gemm_w4a4_pair_kernel, dim3(grid), dim3(THREADS), P_SMEM_BYTES, 2, false, stream, map_a, map_b,
-                     map_y, p);
+    return launch_ex(gemm_w4a4_pair_kernel<EPI>, dim3(grid), dim3(THREADS), P_SMEM_BYTES, 2, false, stream, map_a,
+                     map_b, map_y, p);
   }
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
   const unsigned grid = static_cast<unsigned>(tiles < sm_count() ? tiles : sm_count());
-  gemm_w4a4_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(map_a, map_b, p);
+  gemm_w4a4_kernel<EPI><<<grid, THREADS, SMEM_BYTES, stream>>>(map_a, map_b, p);
   return from_cuda(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_gemm_w4a4(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t* Y, void* ws,
+                     cudaStream_t stream) {
+  return launch_w4a4_epi<EPI_BF16>(A, W, Y, ws, stream, nullptr, nullptr, nullptr, nullptr);
+}
+
+size_t w4a4_quant_workspace_bytes(int64_t M, int64_t N, int64_t K) { return w4a4_workspace_bytes(M, N, K) + 256; }
+
+// W4A4 whose output is handed on as NVFP4 (MMA-layout scales). GIVEN: one
+// fused kernel. COMPUTE: the GEMM writes the bf16 output and its amax, then
+// the quantiser encodes it with s_t = amax / 2688, skipping its own amax pass.
+int launch_gemm_w4a4_quant(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint8_t* codes, uint8_t* scales,
+                           float* s_t, int s_t_mode, uint16_t* Y, void* ws, cudaStream_t stream) {
+  unsigned int* amax = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + w4a4_workspace_bytes(A.rows, W.rows, A.K));
+  if (s_t_mode == NVFP4_ST_GIVEN)
+    return launch_w4a4_epi<EPI_QUANT>(A, W, nullptr, ws, stream, codes, scales, s_t, nullptr);
+  if (cudaMemsetAsync(amax, 0, sizeof(unsigned int), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+  int rc = launch_w4a4_epi<EPI_AMAX>(A, W, Y, ws, stream, nullptr, nullptr, nullptr, amax);
+  if (rc != NVFP4_OK) return rc;
+  return launch_quantize_bf16_from_amax(Y, A.rows, W.rows, codes, scales, amax, s_t, stream);
 }
 
 int read_device_status(int* out, cudaStream_t stream) {

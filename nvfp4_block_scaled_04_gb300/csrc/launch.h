@@ -75,6 +75,10 @@ int launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t
 int launch_prepack_scales(const uint8_t* src, int64_t batch, int64_t rows, int64_t K, uint8_t* dst,
                           cudaStream_t stream);
 size_t quantize_workspace_bytes();
+// bf16 x [rows][K] -> NVFP4 with MMA-layout scales and s_t = amax / 2688,
+// where amax (fp32 bits) was already taken by the kernel that wrote x
+int launch_quantize_bf16_from_amax(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
+                                   const unsigned int* amax_bits, float* s_t, cudaStream_t stream);
 
 // ---- gemv.cu
 size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K);
@@ -103,6 +107,9 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
 size_t w4a4_workspace_bytes(int64_t M, int64_t N, int64_t K);
 int launch_gemm_w4a4(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t* Y, void* ws,
                      cudaStream_t stream);
+size_t w4a4_quant_workspace_bytes(int64_t M, int64_t N, int64_t K);
+int launch_gemm_w4a4_quant(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint8_t* codes, uint8_t* scales,
+                           float* s_t, int s_t_mode, uint16_t* Y, void* ws, cudaStream_t stream);
 int read_device_status(int* out, cudaStream_t stream);
 int selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream);
 int probe_fp4_mma_rate(int n_mma, int n_ctas, cudaStream_t stream);

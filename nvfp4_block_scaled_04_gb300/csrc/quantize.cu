@@ -12,6 +12,7 @@
 // masked speculative decoding head, "What the artifact is").
 #include "common.cuh"
 #include "launch.h"
+#include "quant_core.cuh"
 
 namespace nvfp4 {
 
@@ -74,69 +75,6 @@ __global__ void __launch_bounds__(Q_THREADS) amax_kernel(const T* x, int64_t n8,
     // non-negative floats order like their bit patterns
     atomicMax(out, __float_as_uint(b));
   }
-}
-
-// Packed fp32 pair multiply (both halves rounded to nearest even).
-NVFP4_DEV uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-NVFP4_DEV uint64_t f32_pair(float lo, float hi) {
-  uint64_t d;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
-  return d;
-}
-// Four fp32 pairs (elements 2j, 2j + 1) -> eight e2m1 codes, element j in
-// nibble j (nearest even, saturating at 6, sign kept on a zero magnitude).
-NVFP4_DEV uint32_t e2m1x8_of_pairs(uint64_t p0, uint64_t p1, uint64_t p2, uint64_t p3) {
-  uint32_t out;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .f32 a0, a1, a2, a3, a4, a5, a6, a7;\n\t"
-      "mov.b64 {a0, a1}, %1;\n\tmov.b64 {a2, a3}, %2;\n\tmov.b64 {a4, a5}, %3;\n\tmov.b64 {a6, a7}, %4;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b0, a1, a0;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b1, a3, a2;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b2, a5, a4;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b3, a7, a6;\n\t"
-      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
-      : "=r"(out)
-      : "l"(p0), "l"(p1), "l"(p2), "l"(p3));
-  return out;
-}
-
-// The sixteen codes of one block (two words, element j of each half in nibble
-// j). A code is RNE_e2m1(fl(x / den)) with the sign of x kept on a zero
-// magnitude, and depends only on which side of the e2m1 rounding midpoints
-// the quotient lies. With r = RN(1/den), rh = RN(r (1 + 2^-20)) > 1/den and
-// rl = RN(r (1 - 2^-20)) < 1/den, so RN(|x| rl) <= fl(|x| / den) <= RN(|x| rh)
-// (rounding is monotone), and the code magnitude is monotone in the value:
-// where the products with rl and rh give the same codes, those are the codes
-// of the exact quotients. Otherwise (a quotient at or next to a midpoint) the
-// sixteen quotients are formed by IEEE division.
-NVFP4_DEV uint2 e2m1x16(const float (&v)[16], float den) {
-  if (den > 1e-30f && den < 1e30f) {
-    const float r = __frcp_rn(den);
-    const float rh = __fmul_rn(r, 1.0f + 0x1p-20f), rl = __fmul_rn(r, 1.0f - 0x1p-20f);
-    const uint64_t RH = f32_pair(rh, rh), RL = f32_pair(rl, rl);
-    uint64_t ph[8], pl[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint64_t xv = f32_pair(v[2 * e], v[2 * e + 1]);
-      ph[e] = mul_f32x2(xv, RH);
-      pl[e] = mul_f32x2(xv, RL);
-    }
-    const uint32_t h0 = e2m1x8_of_pairs(ph[0], ph[1], ph[2], ph[3]), h1 = e2m1x8_of_pairs(ph[4], ph[5], ph[6], ph[7]);
-    const uint32_t l0 = e2m1x8_of_pairs(pl[0], pl[1], pl[2], pl[3]), l1 = e2m1x8_of_pairs(pl[4], pl[5], pl[6], pl[7]);
-    if (h0 == l0 && h1 == l1) return make_uint2(h0, h1);
-  }
-  uint2 out;
-  float q[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(v[j], den);
-  out.x = f32x8_to_e2m1x8(q);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(v[8 + j], den);
-  out.y = f32x8_to_e2m1x8(q);
-  return out;
 }
 
 // 16-byte words of one 16-element block: 2 (bf16) or 4 (fp32).
@@ -226,11 +164,8 @@ __global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int6
       if (bi >= bpr) continue;
       float v[16];
       unpack16<T>(raw[u], v);
-      float ab = 0.f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) ab = fmaxf(ab, fabsf(v[e]));
-      const uint32_t sc = f32_to_e4m3(__fdiv_rn(ab, d));
-      const uint2 packed = sc != 0 ? e2m1x16(v, __fmul_rn(e4m3_to_f32(sc), st)) : make_uint2(0u, 0u);
+      uint2 packed;
+      const uint32_t sc = quant_block16(v, st, d, packed);
       reinterpret_cast<uint2*>(codes)[static_cast<int64_t>(row) * bpr + bi] = packed;
       scales[LAYOUT == NVFP4_SCALES_MMA ? srow + (bi >> 2) * 512 + (bi & 3) : srow + bi] = static_cast<uint8_t>(sc);
     }
@@ -314,6 +249,24 @@ int launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t
     else NVFP4_Q(float, NVFP4_SCALES_ROWMAJOR);
   }
 #undef NVFP4_Q
+  return from_cuda(cudaGetLastError());
+}
+
+int launch_quantize_bf16_from_amax(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
+                                   const unsigned int* amax_bits, float* s_t, cudaStream_t stream) {
+  const int64_t cols4 = mma_scale_cols(K);
+  if (rows == 0) return NVFP4_OK;
+  if (rows % 128 != 0 || cols4 != K / 16) {
+    const size_t bytes = static_cast<size_t>(mma_scale_rows(rows) * cols4);
+    if (cudaMemsetAsync(scales, 0, bytes, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+  }
+  if (rows * ((K / 16 + 63) / 64) >= (1LL << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  auto k = quantize_kernel<uint16_t, NVFP4_SCALES_MMA>;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, Q_THREADS, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
+  const int g_max = grid_for(rows * K / 8, Q_THREADS);
+  const int g = g_max < per_sm * sm_count() ? g_max : per_sm * sm_count();
+  k<<<g, Q_THREADS, 0, stream>>>(x, rows, K, codes, scales, amax_bits, s_t, NVFP4_ST_COMPUTE, cols4);
   return from_cuda(cudaGetLastError());
 }
 

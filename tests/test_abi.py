@@ -169,3 +169,19 @@ def test_grouped_workspace_holds_the_tile_table(nv):
     more_experts = nv.workspace_size(nv.OP_GROUPED_GEMM, 4096, H, I, 256, 8)
     assert more_experts > small
     assert nv.workspace_size(nv.OP_GROUPED_GEMM, 4096 + 16, H, I, 128, 8) > small
+
+
+def test_w4a4_quant_validates_arguments(nv):
+    L = nv.lib()
+    ws = _fake(0x20000)
+    A = nv.CTensor(0x30000, 0x40000, 0x50000, 256, 512, 1, 1)
+    W = nv.CTensor(0x60000, 0x70000, 0x80000, 256, 512, 1, 1)
+    Wn = nv.CTensor(0x60000, 0x70000, 0x80000, 200, 512, 1, 1)
+    need = nv.workspace_size(nv.OP_GEMM_W4A4_QUANT, 256, 256, 512)
+    assert need >= 256
+    f = _fake
+    assert L.nvfp4_gemm_w4a4_quant(A, Wn, f(), f(), f(), 1, None, ws, need, None) == -2   # N % 64
+    assert L.nvfp4_gemm_w4a4_quant(A, W, f(), f(), f(), 0, None, ws, need, None) == -1    # COMPUTE needs Y
+    assert L.nvfp4_gemm_w4a4_quant(A, W, f(), f(), f(), 3, None, ws, need, None) == -1    # bad mode
+    assert L.nvfp4_gemm_w4a4_quant(A, W, f(0x1008), f(), f(), 1, None, ws, need, None) == -3   # codes misaligned
+    assert L.nvfp4_gemm_w4a4_quant(A, W, f(), f(), f(), 1, None, ws, need - 1, None) == -5     # workspace
