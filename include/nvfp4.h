@@ -94,6 +94,7 @@ typedef struct nvfp4_tensor {
 #define NVFP4_OP_GROUPED_GEMM    3
 #define NVFP4_OP_GATHER_ARGMAX   4
 #define NVFP4_OP_GEMM_W4A4_QUANT 5
+#define NVFP4_OP_GROUPED_GEMM_W4A4 6
 
 /* ---- entry points ----------------------------------------------------------- */
 
@@ -247,6 +248,28 @@ int nvfp4_grouped_gemm(const void* X, int64_t T, int topk, const int32_t* topk_i
                        void* out, void* workspace, size_t workspace_bytes,
                        nvfp4_stream_t stream);
 
+/* The routed-expert MoE layer of nvfp4_grouped_gemm with 4-bit activations
+ * as well (W4A4 on the block-scaled FP4 tensor cores; What 350+
+ * Experiments..., sections 1 and 7, where the final configuration serves the
+ * experts with an NVFP4 MoE kernel). Readings where the pages are silent:
+ *   - the layer input X is quantised once per call with its own dynamic
+ *     tensor scale (amax / 2688, the quantiser's rules); each routed row is
+ *     its token's quantised row;
+ *   - [g; u] = x_hat @ W13_e^T, h = bf16(silu(g) * u) as in the W4A16 layer;
+ *   - the h rows of all routed (token, slot) pairs are quantised together,
+ *     one dynamic tensor scale per call, before the down projection;
+ *   - out[t] = bf16(sum_j w[t][j] * y[t][j]), fp32, slots in order
+ *     (deterministic).
+ *   X, topk_ids, topk_w, out as for nvfp4_grouped_gemm (an expert id outside
+ *   [0, E) is dropped and reported the same way);
+ *   W13, W2    NVFP4 stacks as for nvfp4_grouped_gemm, with MMA-layout scales
+ *              (nvfp4_prepack_scales, batch = E);
+ *   workspace  >= nvfp4_workspace_size(NVFP4_OP_GROUPED_GEMM_W4A4, T, H, I, E, topk).
+ * H must be a multiple of 256 and I of 128; E <= 4096. */
+int nvfp4_grouped_gemm_w4a4(const void* X, int64_t T, int topk, const int32_t* topk_ids, const float* topk_w,
+                            nvfp4_tensor_t W13, nvfp4_tensor_t W2, void* out, void* workspace,
+                            size_t workspace_bytes, nvfp4_stream_t stream);
+
 /* Masked draft LM head: gathered-row GEMV with a fused argmax. The draft
  * proposes only ids from a fixed subset of the vocabulary, so the head reads
  * only those rows ("The masked head trick", Serving Qwen3.8-27B...):
@@ -325,7 +348,8 @@ size_t nvfp4_scales_bytes(int64_t rows, int64_t K, int scale_layout);
  *   GEMM_W4A4:     (M, N, K, -, -)   (worst case: both operands ROWMAJOR)
  *   GROUPED_GEMM:  (T, H, I, E, topk)
  *   GATHER_ARGMAX: (M, n_idx, K, -, -)
- *   GEMM_W4A4_QUANT: (M, N, K, -, -) */
+ *   GEMM_W4A4_QUANT: (M, N, K, -, -)
+ *   GROUPED_GEMM_W4A4: (T, H, I, E, topk) */
 size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t c, int64_t e, int64_t topk);
 
 /* Human-readable name of a status code (static storage). */

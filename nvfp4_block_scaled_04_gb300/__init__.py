@@ -20,7 +20,8 @@ ERR_INVALID_ARG, ERR_TIMEOUT = -1, -6
 DTYPE_F32, DTYPE_BF16 = 0, 1
 ST_COMPUTE, ST_GIVEN = 0, 1
 SCALES_ROWMAJOR, SCALES_MMA = 0, 1
-OP_QUANTIZE, OP_GEMM_W4A16, OP_GEMM_W4A4, OP_GROUPED_GEMM, OP_GATHER_ARGMAX, OP_GEMM_W4A4_QUANT = range(6)
+(OP_QUANTIZE, OP_GEMM_W4A16, OP_GEMM_W4A4, OP_GROUPED_GEMM, OP_GATHER_ARGMAX, OP_GEMM_W4A4_QUANT,
+ OP_GROUPED_GEMM_W4A4) = range(7)
 
 EXPORTS = [
     "nvfp4_quantize", "nvfp4_prepack_scales", "nvfp4_gemm_w4a16", "nvfp4_gemm_w4a4",
@@ -28,7 +29,7 @@ EXPORTS = [
     "nvfp4_scales_bytes", "nvfp4_workspace_size", "nvfp4_status_string",
     "nvfp4_read_device_status", "nvfp4_selftest_bounded_wait", "nvfp4_version",
     "nvfp4_gemm_w4a16_noalloc", "nvfp4_verify_accept", "nvfp4_probe_fp4_mma_rate",
-    "nvfp4_gemm_w4a16_silu_mul", "nvfp4_gemm_w4a4_quant",
+    "nvfp4_gemm_w4a16_silu_mul", "nvfp4_gemm_w4a4_quant", "nvfp4_grouped_gemm_w4a4",
 ]
 _NON_INT = ("nvfp4_scales_bytes", "nvfp4_workspace_size", "nvfp4_status_string")
 
@@ -60,6 +61,7 @@ def lib() -> ctypes.CDLL:
         L.nvfp4_gemm_w4a16_silu_mul.argtypes = [vp, i64, CTensor, vp, vp, sz, vp]
         L.nvfp4_moe_route.argtypes = [vp, i64, i32, i32, vp, vp, vp]
         L.nvfp4_grouped_gemm.argtypes = [vp, i64, i32, vp, vp, CTensor, CTensor, vp, vp, sz, vp]
+        L.nvfp4_grouped_gemm_w4a4.argtypes = [vp, i64, i32, vp, vp, CTensor, CTensor, vp, vp, sz, vp]
         L.nvfp4_gather_gemv_argmax.argtypes = [vp, i64, CTensor, vp, i64, vp, vp, vp, sz, vp]
         L.nvfp4_gather_rows.argtypes = [CTensor, vp, i64, vp, vp, vp]
         L.nvfp4_gemv_argmax.argtypes = [vp, i64, CTensor, vp, vp, vp, vp, sz, vp]
@@ -256,6 +258,21 @@ def grouped_gemm(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, w13:
         workspace_size(OP_GROUPED_GEMM, T, H, w13.rows // 2, w13.batch, topk), x.device)
     _check(lib().nvfp4_grouped_gemm(_ptr(x), T, topk, _ptr(ids), _ptr(weights), w13.c(), w2.c(), _ptr(o),
                                     _ptr(ws), ws.numel(), _stream()), "nvfp4_grouped_gemm")
+    return o
+
+
+def grouped_gemm_w4a4(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, w13: QTensor, w2: QTensor,
+                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Routed-expert MoE layer with NVFP4 activations (W4A4); w13 / w2 with
+    MMA-layout scales (prepack_scales)."""
+    _require_cuda(x)
+    T, H = x.shape
+    topk = ids.shape[1]
+    o = out if out is not None else torch.empty(T, H, dtype=torch.bfloat16, device=x.device)
+    ws = workspace if workspace is not None else _workspace(
+        workspace_size(OP_GROUPED_GEMM_W4A4, T, H, w13.rows // 2, w13.batch, topk), x.device)
+    _check(lib().nvfp4_grouped_gemm_w4a4(_ptr(x), T, topk, _ptr(ids), _ptr(weights), w13.c(), w2.c(), _ptr(o),
+                                         _ptr(ws), ws.numel(), _stream()), "nvfp4_grouped_gemm_w4a4")
     return o
 
 

@@ -93,6 +93,7 @@ size_t nvfp4_workspace_size(int op, int64_t a, int64_t b, int64_t c, int64_t e, 
     case NVFP4_OP_GEMM_W4A16: return a > 0 && c > 0 ? w4a16_workspace_bytes(a, b, c) : 0;
     case NVFP4_OP_GEMM_W4A4: return w4a4_workspace_bytes(a, b, c);
     case NVFP4_OP_GEMM_W4A4_QUANT: return w4a4_quant_workspace_bytes(a, b, c);
+    case NVFP4_OP_GROUPED_GEMM_W4A4: return grouped_w4a4_workspace_bytes(a, b, c, e, topk);
     case NVFP4_OP_GROUPED_GEMM: return grouped_workspace_bytes(a, b, c, e, topk);
     case NVFP4_OP_GATHER_ARGMAX: return a > 0 && c > 0 ? argmax_workspace_bytes(a, c) : 0;
     default: return 0;
@@ -202,6 +203,24 @@ int nvfp4_grouped_gemm(const void* X, int64_t T, int topk, const int32_t* topk_i
   if (!workspace || workspace_bytes < grouped_workspace_bytes(T, H, I, E, topk)) return NVFP4_ERR_WORKSPACE;
   return launch_grouped_gemm(static_cast<const uint16_t*>(X), T, topk, topk_ids, topk_w, W13, W2,
                              static_cast<uint16_t*>(out), workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int nvfp4_grouped_gemm_w4a4(const void* X, int64_t T, int topk, const int32_t* topk_ids, const float* topk_w,
+                            nvfp4_tensor_t W13, nvfp4_tensor_t W2, void* out, void* workspace, size_t workspace_bytes,
+                            nvfp4_stream_t stream) {
+  if (!X || !topk_ids || !topk_w || !out || T < 0 || topk < 1 || !tensor_ok(W13) || !tensor_ok(W2))
+    return NVFP4_ERR_INVALID_ARG;
+  if (W13.scale_layout != NVFP4_SCALES_MMA || W2.scale_layout != NVFP4_SCALES_MMA) return NVFP4_ERR_INVALID_ARG;
+  const int64_t E = W13.batch, I = W13.rows / 2, H = W13.K;
+  if (W13.rows % 2 != 0 || W2.batch != E || W2.rows != H || W2.K != I || topk > E) return NVFP4_ERR_INVALID_ARG;
+  if (H % 256 != 0 || I % 128 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(X) || !aligned16(out) || !aligned16(W13.codes) || !aligned16(W2.codes) || !aligned16(W13.scales) ||
+      !aligned16(W2.scales))
+    return NVFP4_ERR_MISALIGNED;
+  if (T == 0) return NVFP4_OK;
+  if (!workspace || workspace_bytes < grouped_w4a4_workspace_bytes(T, H, I, E, topk)) return NVFP4_ERR_WORKSPACE;
+  return launch_grouped_gemm_w4a4(static_cast<const uint16_t*>(X), T, topk, topk_ids, topk_w, W13, W2,
+                                  static_cast<uint16_t*>(out), workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int nvfp4_gather_gemv_argmax(const void* H, int64_t M, nvfp4_tensor_t W, const int32_t* idx, int64_t n_idx,

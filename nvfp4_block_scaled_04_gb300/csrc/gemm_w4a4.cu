@@ -809,6 +809,291 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(slot), "r"(32) : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Routed experts with 4-bit activations (W4A4 MoE): a persistent grouped GEMM
+// over the routing plan's tile table, on the same block-scaled FP4 mainloop
+// and warp roles as gemm_w4a4_kernel. The routed rows' NVFP4 codes sit in a
+// tile-major matrix (tile t = up to 128 routed rows of one expert at rows
+// [128 t, 128 t + 128), the rest of the tile zero), so each tile is one TMA
+// box and one strip of the MMA scale layout. Work item w = (tile w / n_tiles,
+// weight block w % n_tiles); the tile count is read on the device.
+//   GATEUP  W13 [E][2I][H]: weight block j = gate rows [128 j, 128 j + 128)
+//           and the matching up rows I + [128 j, ...) in one 256-column
+//           accumulator; epilogue h = bf16(silu(g) * u) into the routed rows'
+//           h buffer (padded row order of the plan) and the largest |h| into
+//           amax_bits (the dynamic tensor scale of the h rows)
+//   DOWN    W2 [E][H][I]: weight block j = rows [256 j, 256 j + 256);
+//           epilogue y (fp32) per routed row for the combine
+struct GroupedW4A4Params {
+  const uint8_t* sfa;             // MMA-layout scales of the tile-major routed rows
+  const uint8_t* sfb;             // MMA-layout scales of each expert matrix, expert e at e * sfb_expert_bytes
+  int64_t sfb_expert_bytes;
+  const float* st_a;              // [1] the routed rows' tensor scale
+  const float* st_b;              // [E] the experts' tensor scales
+  const int* tile_count;
+  const int* tile_expert;
+  const int* tile_row0;           // first row of the tile in the plan's padded row order
+  const int* tile_rows;
+  int K;                          // H (gate/up) or I (down)
+  int n_tiles;                    // weight blocks per tile: I / 128 (gate/up) or H / 256 (down)
+  int rows_per_expert;            // 2I or H
+  int inter;                      // I
+  int hidden;                     // H
+  uint16_t* h_out;                // GATEUP: bf16 [padded rows][I]
+  unsigned int* amax_bits;        // GATEUP: max |h| as fp32 bits (zero on entry)
+  float* y_out;                   // DOWN: fp32 [padded rows][H]
+};
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_w4a4_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                        const GroupedW4A4Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t bar_base = base + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * STAGES + 3);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+  auto sf_bar = [&](int s) { return bar_base + 8u * (2 * STAGES + s); };
+  const uint32_t accf_bar = bar_base + 8u * (3 * STAGES);
+  const uint32_t acce_bar = bar_base + 8u * (3 * STAGES + 1);
+  auto stage_a = [&](int s) { return base + s * STAGE_BYTES; };
+  auto stage_b = [&](int s) { return base + s * STAGE_BYTES + A_BYTES; };
+  auto stage_sfa = [&](int s) { return base + s * STAGE_BYTES + A_BYTES + B_BYTES; };
+  auto stage_sfb = [&](int s) { return base + s * STAGE_BYTES + A_BYTES + B_BYTES + SFA_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_work = *p.tile_count * p.n_tiles;
+  const int n_k = (p.K + BK - 1) / BK;
+  const int k_atoms_total = p.K / 64;
+  const int64_t sf_row_stride = static_cast<int64_t>(k_atoms_total) * 512;   // bytes per 128-row scale strip
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(sf_bar(s), SF_WARPS);
+    }
+    mbar_init(accf_bar, 1);
+    mbar_init(acce_bar, EPI_WARPS);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_a) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_b) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  int next_it = 0;
+  int mma_tiles = 0;
+  const int prod = warp == 0 ? 0 : (warp == 2 ? 1 : -1);
+
+  if (prod >= 0) {
+    if (lane == 0) {
+      int it = 0;
+      for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x) {
+        const int t = w / p.n_tiles, j = w - t * p.n_tiles;
+        const int e = p.tile_expert[t];
+        // the two 128-row weight boxes and their scale strips within expert e
+        const int rb0 = GATEUP ? j : 2 * j;
+        const int rb1 = GATEUP ? p.inter / 128 + j : 2 * j + 1;
+        const int ybase = e * p.rows_per_expert;
+        const uint8_t* sfb_e = p.sfb + static_cast<int64_t>(e) * p.sfb_expert_bytes;
+        bool ok = true;
+        for (int ks = 0; ks < n_k; ++ks, ++it) {
+          if ((it & 1) != prod) continue;
+          const int s = it % STAGES;
+          if (it >= STAGES &&
+              !mbar_wait_bounded(empty_bar(s), ((it / STAGES) - 1) & 1, abort_flag, &g_device_status)) {
+            ok = false;
+            break;
+          }
+          const int atoms = min(4, k_atoms_total - 4 * ks);
+          const uint32_t sf_bytes = static_cast<uint32_t>(atoms) * 512u;
+          mbar_arrive_expect_tx(full_bar(s), A_BYTES + B_BYTES + 3u * sf_bytes);
+          tma_load_2d(stage_a(s), &map_a, ks * 128, t * BM, full_bar(s));
+          tma_load_2d(stage_b(s), &map_b, ks * 128, ybase + rb0 * 128, full_bar(s));
+          tma_load_2d(stage_b(s) + B_BYTES / 2, &map_b, ks * 128, ybase + rb1 * 128, full_bar(s));
+          bulk_load(stage_sfa(s), p.sfa + t * sf_row_stride + static_cast<int64_t>(ks) * 2048, sf_bytes, full_bar(s));
+          bulk_load(stage_sfb(s), sfb_e + rb0 * sf_row_stride + static_cast<int64_t>(ks) * 2048, sf_bytes,
+                    full_bar(s));
+          bulk_load(stage_sfb(s) + 2048, sfb_e + rb1 * sf_row_stride + static_cast<int64_t>(ks) * 2048, sf_bytes,
+                    full_bar(s));
+          next_it = it + 1;
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int it = 0;
+      for (int w = blockIdx.x; w < n_work && !*abort_flag; w += gridDim.x) {
+        if (mma_tiles > 0 && !mbar_wait_bounded(acce_bar, (mma_tiles - 1) & 1, abort_flag, &g_device_status)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int ks = 0; ks < n_k; ++ks, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait_bounded(sf_bar(s), (it / STAGES) & 1, abort_flag, &g_device_status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int atoms = min(4, k_atoms_total - 4 * ks);
+          const uint32_t sf_col = tmem + SF_TMEM_BASE + s * SF_COLS_PER_STAGE;
+          for (int k = 0; k < atoms; ++k) {
+            const uint64_t adesc = smem_desc(stage_a(s) + 32 * k, 16, 1024, 2);
+            const uint64_t bdesc = smem_desc(stage_b(s) + 32 * k, 16, 1024, 2);
+            tc_mma_mxf4nvf4(tmem, adesc, bdesc, IDESC, sf_col + 4 * k, sf_col + 16 + 8 * k,
+                            (ks > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(empty_bar(s));
+        }
+        if (!ok) break;
+        tc_commit(accf_bar);
+        ++mma_tiles;
+      }
+    }
+  } else if (warp < SF_WARP0) {
+    const int quarter = warp & 3;
+    const int half = (warp - EPI_WARP0) >> 2;
+    const int i = quarter * 32 + lane;                 // row within the tile
+    int done = 0;
+    for (int w = blockIdx.x; w < n_work; w += gridDim.x, ++done) {
+      const int t = w / p.n_tiles, j = w - t * p.n_tiles;
+      const int e = p.tile_expert[t];
+      const int nrows = p.tile_rows[t];
+      const int64_t row = static_cast<int64_t>(p.tile_row0[t]) + i;
+      const float scale = p.st_a[0] * p.st_b[e];
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(accf_bar, done & 1, abort_flag, &g_device_status))) break;
+      tc_fence_after();
+      const uint32_t lanes = static_cast<uint32_t>(quarter * 32) << 16;
+      if (GATEUP) {
+        // intermediate columns [64 half, 64 half + 64) of block j: gate at
+        // accumulator columns 64 half + c, up at 128 + 64 half + c
+        uint32_t hv[32];
+        uint32_t hmax = 0u;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t g[32], u[32];
+          tc_ld_32cols(tmem + lanes + static_cast<uint32_t>(64 * half + 32 * c), g);
+          tc_ld_32cols(tmem + lanes + static_cast<uint32_t>(128 + 64 * half + 32 * c), u);
+          tc_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float g0 = __uint_as_float(g[2 * q]) * scale, g1 = __uint_as_float(g[2 * q + 1]) * scale;
+            const float u0 = __uint_as_float(u[2 * q]) * scale, u1 = __uint_as_float(u[2 * q + 1]) * scale;
+            const uint32_t b = f32x2_to_bf16x2(g0 / (1.0f + expf(-g0)) * u0, g1 / (1.0f + expf(-g1)) * u1);
+            hv[16 * c + q] = b;
+            hmax = max(hmax, max(b & 0x7FFFu, (b >> 16) & 0x7FFFu));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar);
+        const bool valid = i < nrows;
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.h_out + row * p.inter + j * 128 + 64 * half);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) dst[q] = make_uint4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+        }
+        const uint32_t m = __reduce_max_sync(0xffffffffu, valid ? hmax : 0u);
+        if (lane == 0 && m != 0u) atomicMax(p.amax_bits, m << 16);
+      } else {
+        // each 32-column chunk is stored as soon as it is read; the
+        // accumulator is released after the last read
+        float4* dst = reinterpret_cast<float4*>(p.y_out + row * p.hidden + j * 256 + half * 128);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tc_ld_32cols(tmem + lanes + static_cast<uint32_t>(half * 128 + 32 * c), r);
+          tc_wait_ld();
+          if (c == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar);
+          }
+          if (i < nrows) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[8 * c + q] = make_float4(__uint_as_float(r[4 * q]) * scale, __uint_as_float(r[4 * q + 1]) * scale,
+                                           __uint_as_float(r[4 * q + 2]) * scale, __uint_as_float(r[4 * q + 3]) * scale);
+          }
+        }
+      }
+    }
+  } else {
+    // scale warps, as in gemm_w4a4_kernel
+    const uint32_t lane_cols = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + SF_TMEM_BASE;
+    int it = 0;
+    for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      bool ok = true;
+      for (int ks = 0; ks < n_k; ++ks, ++it) {
+        const int s = it % STAGES;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_bounded(full_bar(s), (it / STAGES) & 1, abort_flag, &g_device_status))) {
+          ok = false;
+          break;
+        }
+        uint32_t v[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 x = lds128(stage_sfa(s) + 512 * k + 16 * lane);
+          v[4 * k] = x.x, v[4 * k + 1] = x.y, v[4 * k + 2] = x.z, v[4 * k + 3] = x.w;
+        }
+        const uint32_t col = lane_cols + s * SF_COLS_PER_STAGE;
+        tc_st_16cols(col, v);
+#pragma unroll
+        for (int pair = 0; pair < 2; ++pair) {
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint4 x = lds128(stage_sfb(s) + 2048 * h + 512 * (2 * pair + kk) + 16 * lane);
+              const int o = 8 * kk + 4 * h;
+              v[o] = x.x, v[o + 1] = x.y, v[o + 2] = x.z, v[o + 3] = x.w;
+            }
+          tc_st_16cols(col + 16 + 16 * pair, v);
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sf_bar(s));
+      }
+      if (!ok) break;
+    }
+  }
+
+  // Unwind after a give-up: copies and MMAs already issued land (bounded)
+  // before the shared and tensor memory they target go away.
+  if (prod >= 0 && lane == 0 && *abort_flag) {
+    for (int it = next_it - 1; it >= 0 && it >= next_it - 2 * STAGES; --it)
+      if ((it & 1) == prod)
+        mbar_wait_bounded(full_bar(it % STAGES), (it / STAGES) & 1, nullptr, &g_device_status, 100000000ull);
+  }
+  if (warp == 1 && lane == 0 && *abort_flag && mma_tiles > 0) {
+    mbar_wait_bounded(accf_bar, (mma_tiles - 1) & 1, nullptr, &g_device_status, 100000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
 // Issue-rate ceiling of the block-scaled FP4 tensor cores: one CTA per SM
 // issues `n_mma` tcgen05.mma.kind::mxf4nvf4 of 128 x 256 x 64 (the W4A4
 // kernels' instruction) back to back into one accumulator, operands from
@@ -995,6 +1280,49 @@ int read_device_status(int* out, cudaStream_t stream) {
   if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
   *out = v;
   return NVFP4_OK;
+}
+
+int launch_grouped_w4a4(bool gateup, const uint8_t* a_codes, const uint8_t* a_scales, const float* st_a,
+                        int64_t a_rows, const nvfp4_tensor_t& W, const int* tile_count, const int* tile_expert,
+                        const int* tile_row0, const int* tile_rows, int64_t max_tiles, int inter, int hidden,
+                        uint16_t* h_out, unsigned int* amax_bits, float* y_out, cudaStream_t stream) {
+  const int64_t K = W.K, rows = static_cast<int64_t>(W.batch) * W.rows;
+  CUtensorMap map_a, map_b;
+  int rc = make_tmap_2d_u8(&map_a, a_codes, K / 2, a_rows, K / 2, 128, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != NVFP4_OK) return rc;
+  rc = make_tmap_2d_u8(&map_b, W.codes, K / 2, rows, K / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != NVFP4_OK) return rc;
+  GroupedW4A4Params p{};
+  p.sfa = a_scales;
+  p.sfb = W.scales;
+  p.sfb_expert_bytes = mma_scale_rows(W.rows) * mma_scale_cols(K);
+  p.st_a = st_a;
+  p.st_b = W.s_t;
+  p.tile_count = tile_count;
+  p.tile_expert = tile_expert;
+  p.tile_row0 = tile_row0;
+  p.tile_rows = tile_rows;
+  p.K = static_cast<int>(K);
+  p.n_tiles = gateup ? inter / 128 : hidden / 256;
+  p.rows_per_expert = static_cast<int>(W.rows);
+  p.inter = inter;
+  p.hidden = hidden;
+  p.h_out = h_out;
+  p.amax_bits = amax_bits;
+  p.y_out = y_out;
+  // persistent: at most one CTA per SM, fewer when the plan cannot have that many work items
+  const int64_t work_max = max_tiles * p.n_tiles;
+  const unsigned grid = static_cast<unsigned>(work_max < sm_count() ? work_max : sm_count());
+  if (gateup) {
+    rc = ensure_smem(grouped_w4a4_kernel<true>, SMEM_BYTES);
+    if (rc != NVFP4_OK) return rc;
+    grouped_w4a4_kernel<true><<<grid, THREADS, SMEM_BYTES, stream>>>(map_a, map_b, p);
+  } else {
+    rc = ensure_smem(grouped_w4a4_kernel<false>, SMEM_BYTES);
+    if (rc != NVFP4_OK) return rc;
+    grouped_w4a4_kernel<false><<<grid, THREADS, SMEM_BYTES, stream>>>(map_a, map_b, p);
+  }
+  return from_cuda(cudaGetLastError());
 }
 
 int probe_fp4_mma_rate(int n_mma, int n_ctas, cudaStream_t stream) {

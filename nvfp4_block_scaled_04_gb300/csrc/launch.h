@@ -77,6 +77,8 @@ int launch_prepack_scales(const uint8_t* src, int64_t batch, int64_t rows, int64
 size_t quantize_workspace_bytes();
 // bf16 x [rows][K] -> NVFP4 with MMA-layout scales and s_t = amax / 2688,
 // where amax (fp32 bits) was already taken by the kernel that wrote x
+// amax_bits = max |x| (fp32 bits) over n bf16 values (n % 8 == 0); zeroes it first
+int launch_amax_bf16(const uint16_t* x, int64_t n, unsigned int* amax_bits, cudaStream_t stream);
 int launch_quantize_bf16_from_amax(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
                                    const unsigned int* amax_bits, float* s_t, cudaStream_t stream);
 
@@ -102,6 +104,10 @@ size_t grouped_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64
 int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* ids, const float* w,
                         const nvfp4_tensor_t& W13, const nvfp4_tensor_t& W2, uint16_t* out, void* ws,
                         cudaStream_t stream);
+size_t grouped_w4a4_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk);
+int launch_grouped_gemm_w4a4(const uint16_t* X, int64_t T, int topk, const int32_t* ids, const float* w,
+                             const nvfp4_tensor_t& W13, const nvfp4_tensor_t& W2, uint16_t* out, void* ws,
+                             cudaStream_t stream);
 
 // ---- gemm_w4a4.cu
 size_t w4a4_workspace_bytes(int64_t M, int64_t N, int64_t K);
@@ -113,5 +119,11 @@ int launch_gemm_w4a4_quant(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uin
 int read_device_status(int* out, cudaStream_t stream);
 int selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream);
 int probe_fp4_mma_rate(int n_mma, int n_ctas, cudaStream_t stream);
+// Grouped W4A4 expert GEMM over a routing plan's tile table (gate/up with
+// SiLU * mul, or down); a_codes / a_scales: tile-major routed rows [a_rows][K].
+int launch_grouped_w4a4(bool gateup, const uint8_t* a_codes, const uint8_t* a_scales, const float* st_a,
+                        int64_t a_rows, const nvfp4_tensor_t& W, const int* tile_count, const int* tile_expert,
+                        const int* tile_row0, const int* tile_rows, int64_t max_tiles, int inter, int hidden,
+                        uint16_t* h_out, unsigned int* amax_bits, float* y_out, cudaStream_t stream);
 
 }  // namespace nvfp4

@@ -18,6 +18,7 @@
 #include "gemv_tma.cuh"
 #include "launch.h"
 #include "moe_tc.cuh"
+#include "quant_core.cuh"
 
 namespace nvfp4 {
 
@@ -80,12 +81,22 @@ struct MoeWs {
   uint16_t* hbuf;     // [padded rows][I] bf16
   uint4* xfrag2;      // h, K = I
   float* ybuf;        // [padded rows][H] fp32
+  // W4A4 layer: the routed rows as NVFP4 in tile-major order (tile t = rows
+  // [128 t, 128 t + 128)), codes and MMA-layout scales, for x and for h
+  uint8_t* xq_codes;
+  uint8_t* xq_scales;
+  uint8_t* hq_codes;
+  uint8_t* hq_scales;
+  unsigned int* amax;  // [0] x, [1] h (fp32 bits)
+  float* st;           // [0] x, [1] h: the dynamic tensor scales
   size_t bytes;
   int64_t max_chunks;
   int64_t max_tiles;
 };
 
-MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
+// W4A16 (w4a4 false): the plan, the f16 fragment copies and the h / y
+// buffers. W4A4: the plan, h / y and the tile-major NVFP4 routed rows.
+MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk, bool w4a4 = false) {
   MoeWs w{};
   const int64_t R = T * topk;
   w.max_chunks = ceil_div(R, GV_MCHUNK) + E;
@@ -108,14 +119,78 @@ MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
   w.tile_rows = reinterpret_cast<int*>(take(w.max_tiles * sizeof(int)));
   w.row_of = reinterpret_cast<int*>(take(rows * sizeof(int)));
   w.pos_of = reinterpret_cast<int*>(take(R * sizeof(int)));
-  w.pexp1 = reinterpret_cast<int*>(take(rows * sizeof(int)));
-  w.pexp2 = reinterpret_cast<int*>(take(rows * sizeof(int)));
-  w.xfrag1 = reinterpret_cast<uint4*>(take(xfrag_bytes(w.max_chunks, H)));
+  if (!w4a4) {
+    w.pexp1 = reinterpret_cast<int*>(take(rows * sizeof(int)));
+    w.pexp2 = reinterpret_cast<int*>(take(rows * sizeof(int)));
+    w.xfrag1 = reinterpret_cast<uint4*>(take(xfrag_bytes(w.max_chunks, H)));
+  }
   w.hbuf = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(rows) * I * sizeof(uint16_t)));
-  w.xfrag2 = reinterpret_cast<uint4*>(take(xfrag_bytes(w.max_chunks, I)));
+  if (!w4a4) w.xfrag2 = reinterpret_cast<uint4*>(take(xfrag_bytes(w.max_chunks, I)));
   w.ybuf = reinterpret_cast<float*>(take(static_cast<size_t>(rows) * H * sizeof(float)));
+  if (w4a4) {
+    const size_t trows = static_cast<size_t>(w.max_tiles) * 128;
+    w.xq_codes = reinterpret_cast<uint8_t*>(take(trows * H / 2));
+    w.xq_scales = reinterpret_cast<uint8_t*>(take(trows * H / 16));
+    w.hq_codes = reinterpret_cast<uint8_t*>(take(trows * I / 2));
+    w.hq_scales = reinterpret_cast<uint8_t*>(take(trows * I / 16));
+    w.amax = reinterpret_cast<unsigned int*>(take(2 * sizeof(unsigned int)));
+    w.st = reinterpret_cast<float*>(take(2 * sizeof(float)));
+  }
   w.bytes = off;
   return w;
+}
+
+// NVFP4 of the routed rows in tile-major order (the W4A4 expert GEMMs' A
+// operand): one warp per row r = 128 t + i of tile t; rows i < tile_rows[t]
+// hold routed row tile_row0[t] + i of the plan (gather: its token's row of
+// src; else that row of src), the rest of the tile zero codes and scales.
+// The tensor scale is s_t = amax / 2688 (1 if amax is 0), written to
+// *s_t_out; each block takes the quantiser's step (quant_core.cuh).
+constexpr int QR_WARPS = 8;
+__global__ void __launch_bounds__(QR_WARPS * 32) quantize_routed_kernel(const uint16_t* src, int64_t K, bool gather,
+                                                                         const int* row_of, const int* tile_count,
+                                                                         const int* tile_row0, const int* tile_rows,
+                                                                         const unsigned int* amax_bits, float* s_t_out,
+                                                                         uint8_t* codes, uint8_t* scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * QR_WARPS + (threadIdx.x >> 5);
+  const int t = static_cast<int>(r >> 7), i = static_cast<int>(r & 127);
+  if (t >= *tile_count) return;
+  const float amax = __uint_as_float(*amax_bits);
+  const float st = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+  if (r == 0 && lane == 0) *s_t_out = st;
+  const float d = __fmul_rn(st, 6.0f);
+  const uint16_t* srow = nullptr;
+  if (i < tile_rows[t]) {
+    const int64_t pr = static_cast<int64_t>(tile_row0[t]) + i;
+    if (!gather) {
+      srow = src + pr * K;
+    } else {
+      const int tok = row_of[pr];
+      if (tok >= 0) srow = src + static_cast<int64_t>(tok) * K;
+    }
+  }
+  const int nb = static_cast<int>(K / 16);   // a multiple of 4 (K % 64 == 0): no scale-column padding
+  uint2* crow = reinterpret_cast<uint2*>(codes + r * (K / 2));
+  const int64_t srow_off = (r >> 7) * (nb / 4) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+  for (int b = lane; b < nb; b += 32) {
+    uint2 c = make_uint2(0u, 0u);
+    uint32_t sc = 0u;
+    if (srow) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(srow + 16 * b);
+      const uint4 w0 = __ldg(s4), w1 = __ldg(s4 + 1);
+      const uint32_t u[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      float v[16];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v[2 * e] = __uint_as_float(u[e] << 16);
+        v[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+      }
+      sc = quant_block16(v, st, d, c);
+    }
+    crow[b] = c;
+    scales[srow_off + (b >> 2) * 512 + (b & 3)] = static_cast<uint8_t>(sc);
+  }
 }
 
 constexpr int PLAN_MAX_E = 4096;
@@ -471,6 +546,55 @@ int launch_moe_route(const float* logits, int64_t T, int E, int topk, int32_t* i
 
 size_t grouped_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
   return carve_moe(nullptr, T, H, I, E, topk).bytes;
+}
+
+size_t grouped_w4a4_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t topk) {
+  return carve_moe(nullptr, T, H, I, E, topk, true).bytes;
+}
+
+// The routed-expert layer with 4-bit activations (reading R10): the layer
+// input quantised once with its own dynamic tensor scale and gathered per
+// expert tile, the gate/up GEMM on the block-scaled FP4 tensor cores with
+// SiLU * mul and the amax of h fused into its epilogue, every routed h row
+// quantised with one dynamic tensor scale, the down GEMM, and the combine of
+// the W4A16 layer (slots in order, deterministic).
+int launch_grouped_gemm_w4a4(const uint16_t* X, int64_t T, int topk, const int32_t* ids, const float* w,
+                             const nvfp4_tensor_t& W13, const nvfp4_tensor_t& W2, uint16_t* out, void* ws,
+                             cudaStream_t stream) {
+  if (T == 0) return NVFP4_OK;
+  const int64_t E = W13.batch, I = W13.rows / 2, H = W13.K;
+  const int64_t R = T * topk;
+  if (E > PLAN_MAX_E) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  const MoeWs m = carve_moe(ws, T, H, I, E, topk, true);
+  if (m.max_tiles * 128 >= (1LL << 31) / (H / 2)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  route_plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.chunk_count,
+                                            m.chunk_expert, m.chunk_rows, m.tile_count, m.tile_expert, m.tile_row0,
+                                            m.tile_rows, m.row_of, m.pos_of, device_status_ptr());
+  int rc = from_cuda(cudaGetLastError());
+  if (rc != NVFP4_OK) return rc;
+  rc = launch_amax_bf16(X, T * H, m.amax, stream);
+  if (rc != NVFP4_OK) return rc;
+  if (cudaMemsetAsync(m.amax + 1, 0, sizeof(unsigned int), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+  const int64_t trows = m.max_tiles * 128;
+  const unsigned qgrid = static_cast<unsigned>(trows / QR_WARPS);
+  quantize_routed_kernel<<<qgrid, QR_WARPS * 32, 0, stream>>>(X, H, true, m.row_of, m.tile_count, m.tile_row0,
+                                                              m.tile_rows, m.amax, m.st, m.xq_codes, m.xq_scales);
+  rc = from_cuda(cudaGetLastError());
+  if (rc != NVFP4_OK) return rc;
+  rc = launch_grouped_w4a4(true, m.xq_codes, m.xq_scales, m.st, trows, W13, m.tile_count, m.tile_expert, m.tile_row0,
+                           m.tile_rows, m.max_tiles, static_cast<int>(I), static_cast<int>(H), m.hbuf, m.amax + 1,
+                           nullptr, stream);
+  if (rc != NVFP4_OK) return rc;
+  quantize_routed_kernel<<<qgrid, QR_WARPS * 32, 0, stream>>>(m.hbuf, I, false, m.row_of, m.tile_count, m.tile_row0,
+                                                              m.tile_rows, m.amax + 1, m.st + 1, m.hq_codes,
+                                                              m.hq_scales);
+  rc = from_cuda(cudaGetLastError());
+  if (rc != NVFP4_OK) return rc;
+  rc = launch_grouped_w4a4(false, m.hq_codes, m.hq_scales, m.st + 1, trows, W2, m.tile_count, m.tile_expert,
+                           m.tile_row0, m.tile_rows, m.max_tiles, static_cast<int>(I), static_cast<int>(H), nullptr,
+                           nullptr, m.ybuf, stream);
+  if (rc != NVFP4_OK) return rc;
+  return combine(m, w, T, topk, H, out, stream);
 }
 
 int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* ids, const float* w,

@@ -252,6 +252,13 @@ int launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t
   return from_cuda(cudaGetLastError());
 }
 
+int launch_amax_bf16(const uint16_t* x, int64_t n, unsigned int* amax_bits, cudaStream_t stream) {
+  if (cudaMemsetAsync(amax_bits, 0, sizeof(unsigned int), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+  const int64_t n8 = n / 8;
+  if (n8 > 0) amax_kernel<uint16_t><<<grid_for(n8, Q_THREADS), Q_THREADS, 0, stream>>>(x, n8, amax_bits);
+  return from_cuda(cudaGetLastError());
+}
+
 int launch_quantize_bf16_from_amax(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
                                    const unsigned int* amax_bits, float* s_t, cudaStream_t stream) {
   const int64_t cols4 = mma_scale_cols(K);

@@ -50,6 +50,10 @@ Readings where the pages are silent (each is listed in the design doc):
      full-vocabulary argmax there (R6); the drafts are accepted up to the
      first one that differs from the target token at its position, and the
      step emits the accepted drafts plus the target token after them.
+  R12 NVFP4 out    a W4A4 layer whose output feeds the next W4A4 layer hands
+     on the quantisation (R1-R3) of its bf16 output; with a static tensor
+     scale that scale is given, with a dynamic one it is amax/2688 of the
+     whole bf16 output.
   R10 W4A4 MoE     (the routed experts with 4-bit activations as well): the
      layer input is quantised once per call with its own dynamic tensor scale
      and each routed row is its token's quantised row; h as in R7; the h rows
@@ -228,6 +232,13 @@ def gemm_w4a16(x, w: QTensor):
 def gemm_w4a4(a: QTensor, w: QTensor):
     """Y = A_hat @ W_hat^T in fp64 on two quantised operands (R5)."""
     return decode(a) @ decode(w).T
+
+
+def gemm_w4a4_nvfp4(a: QTensor, w: QTensor, s_t=None):
+    """R12: the W4A4 output as NVFP4 for the next W4A4 layer: quantise(bf16(
+    A_hat @ W_hat^T)), tensor scale given or (None) dynamic."""
+    y = bf16_round(gemm_w4a4(a, w)).astype(np.float32)   # bf16 values are exact in fp32
+    return quantize(y, s_t=s_t)
 
 
 def bf16_round(v):

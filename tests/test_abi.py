@@ -171,6 +171,26 @@ def test_grouped_workspace_holds_the_tile_table(nv):
     assert nv.workspace_size(nv.OP_GROUPED_GEMM, 4096 + 16, H, I, 128, 8) > small
 
 
+def test_grouped_gemm_w4a4_validates_arguments(nv):
+    L = nv.lib()
+    ws = _fake(0x20000)
+    E, H, I = 4, 256, 128
+    W13 = nv.CTensor(0x30000, 0x40000, 0x50000, 2 * I, H, E, 1)
+    W2 = nv.CTensor(0x60000, 0x70000, 0x80000, H, I, E, 1)
+    need = nv.workspace_size(nv.OP_GROUPED_GEMM_W4A4, 64, H, I, E, 2)
+    assert need > nv.workspace_size(nv.OP_GROUPED_GEMM_W4A4, 16, H, I, E, 2)
+    args = (_fake(), 64, 2, _fake(), _fake())
+    W13r = nv.CTensor(0x30000, 0x40000, 0x50000, 2 * I, H, E, 0)
+    assert L.nvfp4_grouped_gemm_w4a4(*args, W13r, W2, _fake(), ws, need, None) == -1          # row-major scales
+    W13h = nv.CTensor(0x30000, 0x40000, 0x50000, 2 * I, 128, E, 1)
+    W2h = nv.CTensor(0x60000, 0x70000, 0x80000, 128, I, E, 1)
+    assert L.nvfp4_grouped_gemm_w4a4(*args, W13h, W2h, _fake(), ws, need, None) == -2         # H % 256
+    assert L.nvfp4_grouped_gemm_w4a4(*args, W13, W2, _fake(), ws, need - 1, None) == -5       # workspace
+    W13s = nv.CTensor(0x30000, 0x40008, 0x50000, 2 * I, H, E, 1)
+    assert L.nvfp4_grouped_gemm_w4a4(*args, W13s, W2, _fake(), ws, need, None) == -3          # scales misaligned
+    assert L.nvfp4_grouped_gemm_w4a4(_fake(), 0, 2, _fake(), _fake(), W13, W2, _fake(), None, 0, None) == 0
+
+
 def test_w4a4_quant_validates_arguments(nv):
     L = nv.lib()
     ws = _fake(0x20000)

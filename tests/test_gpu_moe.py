@@ -36,10 +36,20 @@ def moe_case(T, E, H, I, k, seed):
     return logits, x, w13, w2
 
 
+def oracle_routing(logits, k):
+    """The oracle's routing of the router logits, as the grouped GEMM's inputs
+    (int32 ids and fp32 weights on the device) and as the oracle's (numpy).
+    Both sides of a layer comparison take this one routing; the routing
+    kernel is compared with the oracle on its own (test_route_matches_oracle)."""
+    oids, ow = O.moe_route(np.asarray(logits, dtype=np.float32), k)
+    return (torch.from_numpy(oids.astype(np.int32)).to(DEV), torch.from_numpy(ow.astype(np.float32)).to(DEV),
+            oids, ow)
+
+
 def run_gpu(logits, x, w13, w2, k, ids=None, wts=None):
     m = nv()
     if ids is None:
-        ids, wts = m.moe_route(logits.to(DEV), k)
+        ids, wts, _, _ = oracle_routing(logits.numpy(), k)
     q13 = m.quantize_stack([t.to(DEV) for t in w13])
     q2 = m.quantize_stack([t.to(DEV) for t in w2])
     return np_f64(m.grouped_gemm(x.to(DEV), ids, wts, q13, q2)), ids, wts
@@ -48,9 +58,10 @@ def run_gpu(logits, x, w13, w2, k, ids=None, wts=None):
 @pytest.mark.parametrize("T,E,H,I,k", [(16, 4, 128, 128, 2), (100, 8, 256, 128, 3), (37, 16, 128, 256, 8)])
 def test_small_layers(T, E, H, I, k):
     logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=T)
-    out, ids, wts = run_gpu(logits, x, w13, w2, k)
-    ref = O.moe_forward(x.float().numpy(), ids.cpu().numpy(), wts.cpu().numpy().astype(np.float64),
-                        [O.quantize(t.numpy()) for t in w13], [O.quantize(t.numpy()) for t in w2])
+    ids, wts, oids, ow = oracle_routing(logits.numpy(), k)
+    out, _, _ = run_gpu(logits, x, w13, w2, k, ids, wts)
+    ref = O.moe_forward(x.float().numpy(), oids, ow, [O.quantize(t.numpy()) for t in w13],
+                        [O.quantize(t.numpy()) for t in w2])
     assert O.rel_fro(out, ref) <= TOL
 
 
@@ -78,11 +89,10 @@ def test_moe_config_t256_sampled_tokens():
     m = nv()
     T = 256
     logits, x, w13, w2 = synth.moe_inputs(T)
-    ids, wts = m.moe_route(logits.to(DEV), 8)
+    ids, wts, oids, ow = oracle_routing(logits.numpy(), 8)
     q13 = m.quantize_stack([w13[e].to(DEV) for e in range(128)])
     q2 = m.quantize_stack([w2[e].to(DEV) for e in range(128)])
     out = np_f64(m.grouped_gemm(x.to(DEV), ids, wts, q13, q2))
-    oids, ow = O.moe_route(logits.numpy(), 8)
     toks = np.sort(np.random.default_rng(1).choice(T, 64, replace=False))
     used = sorted(set(oids[toks].ravel().tolist()))
     r13 = {e: O.quantize(w13[e].numpy()) for e in used}
@@ -100,9 +110,10 @@ def test_moe_config_t256_sampled_tokens():
                                        (700, 16, 512, 256, 3), (128, 8, 256, 256, 2)])
 def test_tensor_core_layers(T, E, H, I, k):
     logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=T + 1)
-    out, ids, wts = run_gpu(logits, x, w13, w2, k)
-    ref = O.moe_forward(x.float().numpy(), ids.cpu().numpy(), wts.cpu().numpy().astype(np.float64),
-                        [O.quantize(t.numpy()) for t in w13], [O.quantize(t.numpy()) for t in w2])
+    ids, wts, oids, ow = oracle_routing(logits.numpy(), k)
+    out, _, _ = run_gpu(logits, x, w13, w2, k, ids, wts)
+    ref = O.moe_forward(x.float().numpy(), oids, ow, [O.quantize(t.numpy()) for t in w13],
+                        [O.quantize(t.numpy()) for t in w2])
     assert O.rel_fro(out, ref) <= TOL
 
 
@@ -125,11 +136,12 @@ def test_tensor_core_deterministic_and_scaled_tokens():
     logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=13)
     scale = torch.pow(2.0, torch.linspace(-20, 20, T)).unsqueeze(1)
     x = (x.float() * scale).to(torch.bfloat16)
-    a, ids, wts = run_gpu(logits, x, w13, w2, k)
+    ids, wts, oids, ow = oracle_routing(logits.numpy(), k)
+    a, _, _ = run_gpu(logits, x, w13, w2, k, ids, wts)
     b, _, _ = run_gpu(logits, x, w13, w2, k, ids, wts)
     assert np.array_equal(a, b)
-    ref = O.moe_forward(x.float().numpy(), ids.cpu().numpy(), wts.cpu().numpy().astype(np.float64),
-                        [O.quantize(t.numpy()) for t in w13], [O.quantize(t.numpy()) for t in w2])
+    ref = O.moe_forward(x.float().numpy(), oids, ow, [O.quantize(t.numpy()) for t in w13],
+                        [O.quantize(t.numpy()) for t in w2])
     # per-token relative error: the rows span 40 binades
     for t in range(0, T, 37):
         assert O.rel_fro(a[t], ref[t]) <= TOL
@@ -141,11 +153,10 @@ def test_moe_config_t4096_sampled_tokens():
     m = nv()
     T = 4096
     logits, x, w13, w2 = synth.moe_inputs(T)
-    ids, wts = m.moe_route(logits.to(DEV), 8)
+    ids, wts, oids, ow = oracle_routing(logits.numpy(), 8)
     q13 = m.quantize_stack([w13[e].to(DEV) for e in range(128)])
     q2 = m.quantize_stack([w2[e].to(DEV) for e in range(128)])
     out = np_f64(m.grouped_gemm(x.to(DEV), ids, wts, q13, q2))
-    oids, ow = O.moe_route(logits.numpy(), 8)
     toks = np.sort(np.random.default_rng(2).choice(T, 32, replace=False))
     used = sorted(set(oids[toks].ravel().tolist()))
     r13 = {e: O.quantize(w13[e].numpy()) for e in used}
@@ -165,7 +176,7 @@ def test_out_of_range_expert_ids_are_dropped_and_reported(T, E, H, I):
     m = nv()
     k = 2
     logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=T + 7)
-    ids, wts = m.moe_route(logits.to(DEV), k)
+    ids, wts, _, _ = oracle_routing(logits.numpy(), k)
     bad = ids.clone()
     bad[0, 0], bad[3, 1], bad[T - 1, 0] = -2, -1, E
     dropped = wts.clone()
@@ -183,3 +194,77 @@ def test_out_of_range_expert_ids_are_dropped_and_reported(T, E, H, I):
     clean, _, _ = run_gpu(logits, x, w13, w2, k, ok_ids, dropped)
     assert m.read_device_status() == m.OK
     assert O.rel_fro(out, clean) <= TOL
+
+
+# ---------------------------------------------------------------------------
+# The same layer with 4-bit activations (W4A4, reading R10): experts' scales
+# prepacked into the MMA layout, against oracle.moe_forward_w4a4.
+
+def run_gpu_w4a4(x, w13, w2, ids, wts):
+    m = nv()
+    q13 = m.prepack_scales(m.quantize_stack([t.to(DEV) for t in w13]))
+    q2 = m.prepack_scales(m.quantize_stack([t.to(DEV) for t in w2]))
+    return np_f64(m.grouped_gemm_w4a4(x.to(DEV), ids, wts, q13, q2))
+
+
+def ref_w4a4(x, w13, w2, ids, wts):
+    return O.moe_forward_w4a4(x.float().numpy(), ids.cpu().numpy(), wts.cpu().numpy().astype(np.float64),
+                              [O.quantize(t.numpy()) for t in w13], [O.quantize(t.numpy()) for t in w2])
+
+
+@pytest.mark.parametrize("T,E,H,I,k", [(64, 4, 256, 128, 2), (300, 8, 512, 256, 3), (37, 16, 256, 384, 8),
+                                       (1, 4, 256, 128, 1), (700, 4, 256, 256, 2)])
+def test_w4a4_layers(T, E, H, I, k):
+    """Ragged tiles (several 128-row tiles per expert, ragged tails), one
+    token, top-8, I not a multiple of 256 (three-atom last K stage)."""
+    logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=T + 31)
+    ids, wts, _, _ = oracle_routing(logits.numpy(), k)
+    out = run_gpu_w4a4(x, w13, w2, ids, wts)
+    assert O.rel_fro(out, ref_w4a4(x, w13, w2, ids, wts)) <= TOL
+
+
+def test_w4a4_skewed_routing_and_determinism():
+    """600 rows on one expert (five tiles, the last of 88 rows), the others
+    empty; two calls give identical bits."""
+    T, E, H, I = 600, 4, 256, 256
+    logits, x, w13, w2 = moe_case(T, E, H, I, 1, seed=41)
+    ids = torch.full((T, 1), 2, dtype=torch.int32, device=DEV)
+    wts = torch.full((T, 1), 0.75, device=DEV)
+    a = run_gpu_w4a4(x, w13, w2, ids, wts)
+    b = run_gpu_w4a4(x, w13, w2, ids, wts)
+    assert np.array_equal(a, b)
+    assert O.rel_fro(a, ref_w4a4(x, w13, w2, ids, wts)) <= TOL
+
+
+def test_w4a4_out_of_range_expert_ids_are_dropped_and_reported():
+    m = nv()
+    T, E, H, I, k = 96, 4, 256, 128, 2
+    logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=43)
+    ids, wts, _, _ = oracle_routing(logits.numpy(), k)
+    bad = ids.clone()
+    bad[0, 1], bad[5, 0], bad[T - 1, 1] = -2, E, -1
+    m.read_device_status()
+    out = run_gpu_w4a4(x, w13, w2, bad, wts)
+    assert m.read_device_status() == m.ERR_INVALID_ARG
+    assert np.all(np.isfinite(out))
+    assert O.rel_fro(out, ref_w4a4(x, w13, w2, bad, wts)) <= TOL
+
+
+def test_w4a4_moe_config_t4096_sampled_tokens():
+    """The 35B-A3B-shaped layer (128 experts, top-8, H=2048, I=768) at
+    T=4096 with 4-bit activations: the oracle runs the whole layer (the h
+    rows' tensor scale depends on every routed row) with the experts
+    quantised in spawned workers; 64 sampled tokens compared."""
+    from tests.moe_oracle import quantize_experts
+    m = nv()
+    T = 4096
+    logits, x, w13, w2 = synth.moe_inputs(T)
+    ids, wts, oids, ow = oracle_routing(logits.numpy(), 8)
+    q13 = m.prepack_scales(m.quantize_stack([w13[e].to(DEV) for e in range(128)]))
+    q2 = m.prepack_scales(m.quantize_stack([w2[e].to(DEV) for e in range(128)]))
+    out = np_f64(m.grouped_gemm_w4a4(x.to(DEV), ids, wts, q13, q2))
+    r13 = quantize_experts(w13.numpy())
+    r2 = quantize_experts(w2.numpy())
+    ref = O.moe_forward_w4a4(x.float().numpy(), oids, ow, r13, r2)
+    toks = np.sort(np.random.default_rng(3).choice(T, 64, replace=False))
+    assert O.rel_fro(out[toks], ref[toks]) <= TOL

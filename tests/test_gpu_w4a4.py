@@ -122,13 +122,13 @@ def test_quant_epilogue_exact_case_is_bit_exact(M, N, K):
     qa, qw, qa_ref, qw_ref = _exact_operands(M, N, K)
     yb = O.bf16_round(O.gemm_w4a4(qa_ref, qw_ref)).astype(np.float32)
     st_given = np.float32(0.0371)
-    ref = O.quantize(yb, s_t=st_given)
+    ref = O.gemm_w4a4_nvfp4(qa_ref, qw_ref, s_t=st_given)
     q = m.gemm_w4a4_quant(qa, qw, s_t=torch.tensor([float(st_given)]))
     assert np.array_equal(q.codes.cpu().numpy(), ref.codes)
     assert np.array_equal(q.scales.cpu().numpy(), mma_scale_buffer(ref.scales, M, N))
     y = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
     qd = m.gemm_w4a4_quant(qa, qw, y=y)
-    refd = O.quantize(yb)
+    refd = O.gemm_w4a4_nvfp4(qa_ref, qw_ref)
     assert np.float32(qd.s_t.item()) == refd.s_t
     assert np.array_equal(qd.codes.cpu().numpy(), refd.codes)
     assert np.array_equal(qd.scales.cpu().numpy(), mma_scale_buffer(refd.scales, M, N))
@@ -146,9 +146,10 @@ def test_quant_epilogue_general_inputs(M, N, K):
     w = synth.normal_f32((N, K), 0.02, seed=N + 1)
     qa = m.quantize(a.to(DEV), scale_layout=m.SCALES_MMA)
     qw = m.prepack_scales(m.quantize(w.to(DEV)))
-    yb = O.bf16_round(O.gemm_w4a4(O.quantize(a.float().numpy()), O.quantize(w.numpy()))).astype(np.float32)
+    oa, ow = O.quantize(a.float().numpy()), O.quantize(w.numpy())
+    yb = O.bf16_round(O.gemm_w4a4(oa, ow)).astype(np.float32)
     st = np.float32(O.tensor_scale(yb) * np.float32(1.25))
-    ref = O.quantize(yb, s_t=st)
+    ref = O.gemm_w4a4_nvfp4(oa, ow, s_t=st)
     q = m.gemm_w4a4_quant(qa, qw, s_t=torch.tensor([float(st)]))
     from tests.gpu_common import unpack_mma_scales
     got = O.QTensor(q.codes.cpu().numpy(), unpack_mma_scales(q.scales.cpu().numpy(), M, N), st)
