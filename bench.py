@@ -495,7 +495,8 @@ def measure_rows(nv, peaks, reps):
     E, H, I, k = 128, 2048, 768, 8
     w13 = nv.quantize_stack([gpu_normal((2 * I, H), 0.02, seed=1000 + e) for e in range(E)])
     w2 = nv.quantize_stack([gpu_normal((H, I), 0.02, seed=2000 + e) for e in range(E)])
-    moe = {}
+    w13m, w2m = nv.prepack_scales(w13), nv.prepack_scales(w2)   # MMA-layout scales for the W4A4 layer
+    moe, moe4 = {}, {}
     wbytes = E * (2 * I * H + H * I) * (1 / 2 + 1 / 16)
     for T in (256, 4096):
         logits = gpu_normal((T, E), 1.0, seed=8)
@@ -512,7 +513,18 @@ def measure_rows(nv, peaks, reps):
         b = wbytes + 4 * T * H
         moe[f"T{T}"] = {"ms": t, "gbs": b / t / 1e6, "frac_hbm": b / t / 1e6 / peaks["hbm_gbs"],
                         "tflops": flops / t / 1e9, "frac_bf16_peak": flops / t / 1e9 / peaks["bf16_tflops"]}
+        ws4 = torch.empty(nv.workspace_size(nv.OP_GROUPED_GEMM_W4A4, T, H, I, E, k), dtype=torch.uint8, device="cuda")
+
+        def layer4():
+            ids, wts = nv.moe_route(logits, k)
+            nv.grouped_gemm_w4a4(x, ids, wts, w13m, w2m, out=o, workspace=ws4)
+        g4 = capture(layer4)
+        t4 = time_graph(g4, reps, flush=flush)
+        moe4[f"T{T}"] = {"ms": t4, "gbs": b / t4 / 1e6, "frac_hbm": b / t4 / 1e6 / peaks["hbm_gbs"],
+                         "tflops": flops / t4 / 1e9, "frac_fp4_ceiling_measured": flops / t4 / 1e9 / probe_tflops}
+        del g4, ws4
     out["moe"] = moe
+    out["moe_w4a4"] = moe4
     return out
 
 
