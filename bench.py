@@ -782,7 +782,7 @@ def run_case(args):
     elif args.case == "quantize":
         M, K = args.m, 5120
         a = gpu_student_t((M, K), 4, seed=3)
-        ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+        ws = torch.empty(nv.workspace_size(nv.OP_QUANTIZE, M, 0, K), dtype=torch.uint8, device="cuda")
         g = capture(lambda: nv.quantize(a, scale_layout=nv.SCALES_MMA, workspace=ws))
         res.update(shape=[M, K], ms=time_graph(g, 3))
     elif args.case == "draft":

@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "quant_core.cuh"
+#include "tc_util.cuh"
 
 namespace nvfp4 {
 
@@ -42,18 +43,55 @@ NVFP4_DEV void load8<float>(const float* p, float (&v)[8]) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// Four 8-element loads in flight per thread; the pass walks the tensor from
-// its start to its end, so its last part is what the L2 holds afterwards.
+// 16-byte load kept in L2 with the given policy (the quantise pass reads the
+// same bytes again right after the amax pass).
+NVFP4_DEV uint4 ld_hint_v4(const void* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
 template <typename T>
-__global__ void __launch_bounds__(Q_THREADS) amax_kernel(const T* x, int64_t n8, unsigned int* out) {
+NVFP4_DEV void load8_keep(const T* p, float (&v)[8], uint64_t policy);
+template <>
+NVFP4_DEV void load8_keep<uint16_t>(const uint16_t* p, float (&v)[8], uint64_t policy) {
+  const uint4 u = ld_hint_v4(p, policy);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    v[2 * e] = bf16_bits_to_f32(w[e] & 0xFFFFu);
+    v[2 * e + 1] = bf16_bits_to_f32(w[e] >> 16);
+  }
+}
+template <>
+NVFP4_DEV void load8_keep<float>(const float* p, float (&v)[8], uint64_t policy) {
+  const uint4 a = ld_hint_v4(p, policy), b = ld_hint_v4(p + 4, policy);
+  v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+  v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+}
+
+// The amax pass: CTA b writes the largest |x| of its share to partial[b]
+// (fp32 bits; non-negative floats order like their bit patterns), so nothing
+// has to be zeroed before it; with ATOMIC, every CTA folds its maximum into
+// partial[0] instead (zeroed by the caller). Four 8-element loads in flight per thread, kept
+// in L2 (evict-last) for the quantise pass; the pass walks the tensor from
+// its start to its end. The quantise pass is launched as its programmatic
+// dependent: it may start (and load its first blocks) once every CTA of
+// this pass has started.
+template <typename T, bool ATOMIC = false>
+__global__ void __launch_bounds__(Q_THREADS) amax_kernel(const T* x, int64_t n8, unsigned int* partial) {
   __shared__ float red[Q_THREADS / 32];
+  pdl_launch_dependents();
+  uint64_t keep;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
   float m = 0.f;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   for (; i + 3 * stride < n8; i += 4 * stride) {
     float v[4][8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) load8<T>(x + (i + u * stride) * 8, v[u]);
+    for (int u = 0; u < 4; ++u) load8_keep<T>(x + (i + u * stride) * 8, v[u], keep);
 #pragma unroll
     for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -61,7 +99,7 @@ __global__ void __launch_bounds__(Q_THREADS) amax_kernel(const T* x, int64_t n8,
   }
   for (; i < n8; i += stride) {
     float v[8];
-    load8<T>(x + i * 8, v);
+    load8_keep<T>(x + i * 8, v, keep);
 #pragma unroll
     for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[e]));
   }
@@ -72,8 +110,8 @@ __global__ void __launch_bounds__(Q_THREADS) amax_kernel(const T* x, int64_t n8,
   if (threadIdx.x == 0) {
     float b = 0.f;
     for (int w = 0; w < Q_THREADS / 32; ++w) b = fmaxf(b, red[w]);
-    // non-negative floats order like their bit patterns
-    atomicMax(out, __float_as_uint(b));
+    if (ATOMIC) atomicMax(partial, __float_as_uint(b));
+    else partial[blockIdx.x] = __float_as_uint(b);
   }
 }
 
@@ -117,22 +155,20 @@ NVFP4_DEV void unpack16<float>(const uint4 (&w)[4], float (&v)[16]) {
 // column part: byte (row, col) of the layout with `cols4` (padded K/16)
 // columns is tile * 512 + (row % 32) * 16 + ((row / 32) % 4) * 4 + col % 4,
 // tile = (row / 128) * (cols4 / 4) + col / 4.
+//
+// Tensor scale: GIVEN reads *s_t; COMPUTE takes s_t = amax / 2688 (1 if amax
+// is 0) with amax the largest of amax_bits[0 .. n_amax) (the amax pass's
+// per-CTA maxima, or one value). In COMPUTE the kernel may run as the amax
+// pass's programmatic dependent: its first blocks are loaded before it waits
+// for that pass's results.
 template <typename T, int LAYOUT>
 __global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int64_t rows, int64_t K,
                                                                  uint8_t* codes, uint8_t* scales,
-                                                                 const unsigned int* amax_bits, float* s_t,
-                                                                 int mode, int64_t cols4) {
+                                                                 const unsigned int* amax_bits, int n_amax,
+                                                                 float* s_t, int mode, int64_t cols4) {
   constexpr int NW = BlockWords<T>::N;
   constexpr int BPT = 4 / NW;   // 2 blocks (bf16) or 1 (fp32) per thread
-  float st;
-  if (mode == NVFP4_ST_COMPUTE) {
-    const float amax = __uint_as_float(*amax_bits);
-    st = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *s_t = st;
-  } else {
-    st = *s_t;
-  }
-  const float d = __fmul_rn(st, 6.0f);
+  __shared__ unsigned int s_amax;
   // chunk indices fit in 32 bits (checked at launch)
   const uint32_t bpr = static_cast<uint32_t>(K / 16);
   const int cpr = static_cast<int>((bpr + 32 * BPT - 1) / (32 * BPT));
@@ -140,14 +176,13 @@ __global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int6
   const int warps = static_cast<int>(gridDim.x * (blockDim.x / 32));
   const int n_chunks = static_cast<int>(rows * cpr);
   const int c0 = n_chunks - 1 - static_cast<int>(blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5));
-  if (c0 < 0) return;
-  int row = c0 / cpr, cc = c0 - row * cpr;
+  int row = c0 >= 0 ? c0 / cpr : -1, cc = c0 >= 0 ? c0 - row * cpr : 0;
   const int drow = warps / cpr, dcc = warps - drow * cpr;
   const int64_t tiles_per_row = cols4 >> 2;
-  while (row >= 0) {
+  uint4 raw[BPT][NW];
+  auto load_chunk = [&]() {
     const uint32_t b0 = static_cast<uint32_t>(cc) * (32 * BPT) + lane;
     const T* xrow = x + static_cast<int64_t>(row) * K;
-    uint4 raw[BPT][NW];
 #pragma unroll
     for (int u = 0; u < BPT; ++u) {
       const uint32_t bi = b0 + 32 * u;
@@ -155,6 +190,27 @@ __global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int6
 #pragma unroll
       for (int i = 0; i < NW; ++i) raw[u][i] = __ldg(src + i);
     }
+  };
+  if (row >= 0) load_chunk();
+  float st;
+  if (mode == NVFP4_ST_COMPUTE) {
+    pdl_wait();   // the amax pass's maxima are complete and visible
+    if (threadIdx.x == 0) s_amax = 0u;
+    __syncthreads();
+    unsigned int m = 0u;
+    for (int i = threadIdx.x; i < n_amax; i += blockDim.x) m = max(m, __ldcg(amax_bits + i));
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (lane == 0) atomicMax(&s_amax, m);
+    __syncthreads();
+    const float amax = __uint_as_float(s_amax);
+    st = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *s_t = st;
+  } else {
+    st = *s_t;
+  }
+  const float d = __fmul_rn(st, 6.0f);
+  while (row >= 0) {
+    const uint32_t b0 = static_cast<uint32_t>(cc) * (32 * BPT) + lane;
     const int64_t srow = LAYOUT == NVFP4_SCALES_MMA
                              ? (static_cast<int64_t>(row >> 7) * tiles_per_row) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4
                              : static_cast<int64_t>(row) * bpr;
@@ -175,6 +231,7 @@ __global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int6
       cc += cpr;
       row -= 1;
     }
+    if (row >= 0) load_chunk();
   }
 }
 
@@ -204,7 +261,9 @@ int grid_for(int64_t work, int threads) {
 
 }  // namespace
 
-size_t quantize_workspace_bytes() { return 256; }
+// the amax pass's per-CTA maxima: at most AMAX_MAX_CTAS of them
+constexpr int AMAX_MAX_CTAS = 2048;
+size_t quantize_workspace_bytes() { return AMAX_MAX_CTAS * sizeof(unsigned int); }
 
 int launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t* codes, uint8_t* scales,
                     float* s_t, int s_t_mode, int scale_layout, void* workspace, cudaStream_t stream) {
@@ -215,21 +274,22 @@ int launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t
     const size_t bytes = static_cast<size_t>(mma_scale_rows(rows) * cols4);
     if (cudaMemsetAsync(scales, 0, bytes, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
   }
+  int n_amax = 0;
   if (s_t_mode == NVFP4_ST_COMPUTE) {
-    if (cudaMemsetAsync(amax, 0, sizeof(unsigned int), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
-    if (n8 > 0) {
-      const int g = grid_for(n8, Q_THREADS);
-      if (x_dtype == NVFP4_DTYPE_BF16)
-        amax_kernel<uint16_t><<<g, Q_THREADS, 0, stream>>>(static_cast<const uint16_t*>(x), n8, amax);
-      else
-        amax_kernel<float><<<g, Q_THREADS, 0, stream>>>(static_cast<const float*>(x), n8, amax);
-    }
+    n_amax = grid_for(n8 > 0 ? n8 : 1, Q_THREADS);
+    if (n_amax > AMAX_MAX_CTAS) n_amax = AMAX_MAX_CTAS;
+    if (x_dtype == NVFP4_DTYPE_BF16)
+      amax_kernel<uint16_t><<<n_amax, Q_THREADS, 0, stream>>>(static_cast<const uint16_t*>(x), n8, amax);
+    else
+      amax_kernel<float><<<n_amax, Q_THREADS, 0, stream>>>(static_cast<const float*>(x), n8, amax);
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   }
   if (rows * ((K / 16 + 63) / 64) >= (1LL << 30)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   // one full wave of resident blocks (the chunks are walked with a grid
   // stride): a grid of 8 blocks per SM at 6 resident left a quarter of the
   // work to a second, partial wave
   const int g_max = grid_for(n8 > 0 ? n8 : 1, Q_THREADS);
+  int rc = NVFP4_OK;
 #define NVFP4_Q(T, L)                                                                                         \
   do {                                                                                                        \
     int per_sm = 0;                                                                                           \
@@ -238,8 +298,9 @@ int launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t
         per_sm < 1)                                                                                           \
       per_sm = 1;                                                                                             \
     const int g = g_max < per_sm * sm_count() ? g_max : per_sm * sm_count();                                  \
-    quantize_kernel<T, L><<<g, Q_THREADS, 0, stream>>>(static_cast<const T*>(x), rows, K, codes, scales, amax, \
-                                                       s_t, s_t_mode, cols4);                                 \
+    rc = launch_ex(quantize_kernel<T, L>, dim3(g), dim3(Q_THREADS), 0, 1, s_t_mode == NVFP4_ST_COMPUTE, stream,  \
+                   static_cast<const T*>(x), rows, K, codes, scales, static_cast<const unsigned int*>(amax),    \
+                   n_amax, s_t, s_t_mode, cols4);                                                             \
   } while (0)
   if (x_dtype == NVFP4_DTYPE_BF16) {
     if (scale_layout == NVFP4_SCALES_MMA) NVFP4_Q(uint16_t, NVFP4_SCALES_MMA);
@@ -249,13 +310,13 @@ int launch_quantize(const void* x, int x_dtype, int64_t rows, int64_t K, uint8_t
     else NVFP4_Q(float, NVFP4_SCALES_ROWMAJOR);
   }
 #undef NVFP4_Q
-  return from_cuda(cudaGetLastError());
+  return rc;
 }
 
 int launch_amax_bf16(const uint16_t* x, int64_t n, unsigned int* amax_bits, cudaStream_t stream) {
   if (cudaMemsetAsync(amax_bits, 0, sizeof(unsigned int), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
   const int64_t n8 = n / 8;
-  if (n8 > 0) amax_kernel<uint16_t><<<grid_for(n8, Q_THREADS), Q_THREADS, 0, stream>>>(x, n8, amax_bits);
+  if (n8 > 0) amax_kernel<uint16_t, true><<<grid_for(n8, Q_THREADS), Q_THREADS, 0, stream>>>(x, n8, amax_bits);
   return from_cuda(cudaGetLastError());
 }
 
@@ -273,7 +334,7 @@ int launch_quantize_bf16_from_amax(const uint16_t* x, int64_t rows, int64_t K, u
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, Q_THREADS, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
   const int g_max = grid_for(rows * K / 8, Q_THREADS);
   const int g = g_max < per_sm * sm_count() ? g_max : per_sm * sm_count();
-  k<<<g, Q_THREADS, 0, stream>>>(x, rows, K, codes, scales, amax_bits, s_t, NVFP4_ST_COMPUTE, cols4);
+  k<<<g, Q_THREADS, 0, stream>>>(x, rows, K, codes, scales, amax_bits, 1, s_t, NVFP4_ST_COMPUTE, cols4);
   return from_cuda(cudaGetLastError());
 }
 
