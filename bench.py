@@ -794,16 +794,19 @@ def run_case(args):
         h = gpu_normal((args.m, K), 1.0, seed=7, dtype=torch.bfloat16)
         g = capture(lambda: nv.gather_gemv_argmax(h, qh, idx))
         res.update(M=args.m, ms=time_graph(g, 3))
-    elif args.case == "moe":
+    elif args.case in ("moe", "moe_w4a4"):
         E, H, I = 128, 2048, 768
         w13 = nv.quantize_stack([gpu_normal((2 * I, H), 0.02, seed=1000 + e) for e in range(E)])
         w2 = nv.quantize_stack([gpu_normal((H, I), 0.02, seed=2000 + e) for e in range(E)])
+        if args.case == "moe_w4a4":
+            w13, w2 = nv.prepack_scales(w13), nv.prepack_scales(w2)
         logits = gpu_normal((args.m, E), 1.0, seed=8)
         x = gpu_normal((args.m, H), 1.0, seed=9, dtype=torch.bfloat16)
+        fn = nv.grouped_gemm_w4a4 if args.case == "moe_w4a4" else nv.grouped_gemm
 
         def layer():
             ids, wts = nv.moe_route(logits, 8)
-            nv.grouped_gemm(x, ids, wts, w13, w2)
+            fn(x, ids, wts, w13, w2)
         g = capture(layer)
         res.update(T=args.m, ms=time_graph(g, 3))
     torch.cuda.synchronize()
@@ -820,7 +823,7 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the non-headline rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work per core for cpu_baseline")
-    ap.add_argument("--case", choices=["w4a4", "quantize", "draft", "moe"], default=None,
+    ap.add_argument("--case", choices=["w4a4", "quantize", "draft", "moe", "moe_w4a4"], default=None,
                     help="run one kernel family only (the profiling workloads)")
     ap.add_argument("--m", type=int, default=2048, help="rows / tokens for --case")
     # the oracle child processes of the CPU legs
