@@ -226,7 +226,8 @@ int nvfp4_moe_route(const float* logits, int64_t T, int E, int topk,
  *   for each token t and slot j with e = topk_ids[t][j]:
  *     [g; u] = X[t] @ W13_e^T      (W13_e rows [0, I) gate, [I, 2I) up)
  *     h      = bf16( silu(g) * u )
- *     out[t] += topk_w[t][j] * (h @ W2_e^T)
+ *     y      = bf16( h @ W2_e^T )  (fp32 accumulation)
+ *     out[t] += topk_w[t][j] * y
  *   out = bf16(sum over j, fp32, in slot order).
  *   X        device bf16 [T][H];  topk_ids int32 [T][topk]: a slot whose id
  *            lies outside [0, E) is dropped (it adds nothing to out[t]) and

@@ -823,7 +823,7 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns) {
 //           h buffer (padded row order of the plan) and the largest |h| into
 //           amax_bits (the dynamic tensor scale of the h rows)
 //   DOWN    W2 [E][H][I]: weight block j = rows [256 j, 256 j + 256);
-//           epilogue y (fp32) per routed row for the combine
+//           epilogue y (bf16) per routed row for the combine
 struct GroupedW4A4Params {
   const uint8_t* sfa;             // MMA-layout scales of the tile-major routed rows
   const uint8_t* sfb;             // MMA-layout scales of each expert matrix, expert e at e * sfb_expert_bytes
@@ -841,7 +841,7 @@ struct GroupedW4A4Params {
   int hidden;                     // H
   uint16_t* h_out;                // GATEUP: bf16 [padded rows][I]
   unsigned int* amax_bits;        // GATEUP: max |h| as fp32 bits (zero on entry)
-  float* y_out;                   // DOWN: fp32 [padded rows][H]
+  uint16_t* y_out;                // DOWN: bf16 [padded rows][H]
 };
 
 template <bool GATEUP>
@@ -994,7 +994,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int q = 0; q < 16; ++q) {
             const float g0 = __uint_as_float(g[2 * q]) * scale, g1 = __uint_as_float(g[2 * q + 1]) * scale;
             const float u0 = __uint_as_float(u[2 * q]) * scale, u1 = __uint_as_float(u[2 * q + 1]) * scale;
-            const uint32_t b = f32x2_to_bf16x2(g0 / (1.0f + expf(-g0)) * u0, g1 / (1.0f + expf(-g1)) * u1);
+            // silu with the fast exponential and division (relative error ~1e-7,
+            // far below the bf16 rounding of h); this math sits between the MMAs
+            // of one work item and the next, since the accumulator is not double
+            // buffered (tensor memory is full)
+            const uint32_t b = f32x2_to_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
+                                               __fdividef(g1, 1.0f + __expf(-g1)) * u1);
             hv[16 * c + q] = b;
             hmax = max(hmax, max(b & 0x7FFFu, (b >> 16) & 0x7FFFu));
           }
@@ -1013,7 +1018,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       } else {
         // each 32-column chunk is stored as soon as it is read; the
         // accumulator is released after the last read
-        float4* dst = reinterpret_cast<float4*>(p.y_out + row * p.hidden + j * 256 + half * 128);
+        uint4* dst = reinterpret_cast<uint4*>(p.y_out + row * p.hidden + j * 256 + half * 128);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
@@ -1026,9 +1031,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           if (i < nrows) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[8 * c + q] = make_float4(__uint_as_float(r[4 * q]) * scale, __uint_as_float(r[4 * q + 1]) * scale,
-                                           __uint_as_float(r[4 * q + 2]) * scale, __uint_as_float(r[4 * q + 3]) * scale);
+            for (int q = 0; q < 4; ++q) {
+              uint32_t b[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                b[e] = f32x2_to_bf16x2(__uint_as_float(r[8 * q + 2 * e]) * scale,
+                                       __uint_as_float(r[8 * q + 2 * e + 1]) * scale);
+              dst[4 * c + q] = make_uint4(b[0], b[1], b[2], b[3]);
+            }
           }
         }
       }
@@ -1285,7 +1295,7 @@ int read_device_status(int* out, cudaStream_t stream) {
 int launch_grouped_w4a4(bool gateup, const uint8_t* a_codes, const uint8_t* a_scales, const float* st_a,
                         int64_t a_rows, const nvfp4_tensor_t& W, const int* tile_count, const int* tile_expert,
                         const int* tile_row0, const int* tile_rows, int64_t max_tiles, int inter, int hidden,
-                        uint16_t* h_out, unsigned int* amax_bits, float* y_out, cudaStream_t stream) {
+                        uint16_t* h_out, unsigned int* amax_bits, uint16_t* y_out, cudaStream_t stream) {
   const int64_t K = W.K, rows = static_cast<int64_t>(W.batch) * W.rows;
   CUtensorMap map_a, map_b;
   int rc = make_tmap_2d_u8(&map_a, a_codes, K / 2, a_rows, K / 2, 128, BM, CU_TENSOR_MAP_SWIZZLE_128B);

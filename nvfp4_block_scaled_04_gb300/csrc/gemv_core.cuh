@@ -255,7 +255,7 @@ struct SkinnyParams {
   int64_t hidden;              // H
   int64_t rows_per_expert;     // rows of one expert matrix
   uint16_t* h_out;             // GATEUP: bf16 [padded rows][I]
-  float* y_out;                // DOWN: fp32 [padded rows][H]
+  uint16_t* y_out;             // DOWN: bf16 [padded rows][H]
 };
 
 template <int NT, int MODE>
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(GV_THREADS, 2) skinny_kernel(const SkinnyParam
       p.h_out[(row_base + tok) * p.inter + row_tile * 64 + r] = static_cast<uint16_t>(f32_to_bf16_bits(hh));
     } else {
       const int64_t c = row_tile * GV_ROWS + r;
-      if (c < p.hidden) p.y_out[(row_base + tok) * p.hidden + c] = v * mul;
+      if (c < p.hidden) p.y_out[(row_base + tok) * p.hidden + c] = static_cast<uint16_t>(f32_to_bf16_bits(v * mul));
     }
   }
   if (S > 1) cluster_sync_all();

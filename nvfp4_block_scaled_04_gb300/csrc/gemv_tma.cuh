@@ -73,7 +73,7 @@ struct TmaSkinnyParams {
   int64_t hidden;
   int64_t rows_per_expert;
   uint16_t* h_out;
-  float* y_out;
+  uint16_t* y_out;             // MOE_DOWN: bf16 [padded rows][H]
   int* status;
   float* partials;             // split-K > 1: [tile][split][32 tokens][128 rows] fp32
   unsigned int* counters;      // split-K > 1: one arrival counter per tile, zeroed by the prep kernel
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
           p.h_out[(row_base + tok) * p.inter + row_tile * 64 + r] = static_cast<uint16_t>(f32_to_bf16_bits(hh));
         } else {
           const int64_t c = row_tile * GV_ROWS + r;
-          if (c < p.hidden) p.y_out[(row_base + tok) * p.hidden + c] = v * mul;
+          if (c < p.hidden) p.y_out[(row_base + tok) * p.hidden + c] = static_cast<uint16_t>(f32_to_bf16_bits(v * mul));
         }
       }
       if (MODE == SK_ARGMAX) {

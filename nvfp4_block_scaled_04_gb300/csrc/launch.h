@@ -124,6 +124,6 @@ int probe_fp4_mma_rate(int n_mma, int n_ctas, cudaStream_t stream);
 int launch_grouped_w4a4(bool gateup, const uint8_t* a_codes, const uint8_t* a_scales, const float* st_a,
                         int64_t a_rows, const nvfp4_tensor_t& W, const int* tile_count, const int* tile_expert,
                         const int* tile_row0, const int* tile_rows, int64_t max_tiles, int inter, int hidden,
-                        uint16_t* h_out, unsigned int* amax_bits, float* y_out, cudaStream_t stream);
+                        uint16_t* h_out, unsigned int* amax_bits, uint16_t* y_out, cudaStream_t stream);
 
 }  // namespace nvfp4

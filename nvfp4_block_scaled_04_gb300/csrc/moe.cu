@@ -6,11 +6,11 @@
 //             multiple of 32 rows (one token chunk of the skinny kernel), in
 //             one single-CTA kernel
 //   gate/up:  [g; u] = x @ W13_e^T, h = bf16(silu(g) * u)
-//   down:     y = h @ W2_e^T, fp32
+//   down:     y = bf16(h @ W2_e^T) (fp32 accumulation)
 // (both on the TMA-fed skinny kernel when K is a multiple of 256, else on the
 // register-fed one; with at least XT_MIN_ROWS_PER_EXPERT routed rows per
 // expert on average, on the tensor cores instead: moe_tc.cuh)
-//   combine:  out[t] = bf16(sum_j w[t][j] * y[pos(t, j)]), slots in order
+//   combine:  out[t] = bf16(sum_j w[t][j] * y[pos(t, j)]) in fp32, slots in order
 // The order in which routed rows land inside an expert's group comes from
 // atomics, but every row's arithmetic is independent of its position, so the
 // output is deterministic.
@@ -80,11 +80,14 @@ struct MoeWs {
   uint4* xfrag1;      // tokens, K = H
   uint16_t* hbuf;     // [padded rows][I] bf16
   uint4* xfrag2;      // h, K = I
-  float* ybuf;        // [padded rows][H] fp32
+  uint16_t* ybuf;     // [padded rows][H] bf16: each routed row's expert output
   // W4A4 layer: the routed rows as NVFP4 in tile-major order (tile t = rows
   // [128 t, 128 t + 128)), codes and MMA-layout scales, for x and for h
   uint8_t* xq_codes;
   uint8_t* xq_scales;
+  uint8_t* xt_codes;   // the layer input quantised once per token: [T][H/2]
+  uint8_t* xt_scales;  // [T][H/16], row-major
+  void* q_ws;          // the quantiser's workspace
   uint8_t* hq_codes;
   uint8_t* hq_scales;
   unsigned int* amax;  // [0] x, [1] h (fp32 bits)
@@ -126,9 +129,12 @@ MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
   }
   w.hbuf = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(rows) * I * sizeof(uint16_t)));
   if (!w4a4) w.xfrag2 = reinterpret_cast<uint4*>(take(xfrag_bytes(w.max_chunks, I)));
-  w.ybuf = reinterpret_cast<float*>(take(static_cast<size_t>(rows) * H * sizeof(float)));
+  w.ybuf = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(rows) * H * sizeof(uint16_t)));
   if (w4a4) {
     const size_t trows = static_cast<size_t>(w.max_tiles) * 128;
+    w.xt_codes = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * H / 2));
+    w.xt_scales = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * H / 16));
+    w.q_ws = take(quantize_workspace_bytes());
     w.xq_codes = reinterpret_cast<uint8_t*>(take(trows * H / 2));
     w.xq_scales = reinterpret_cast<uint8_t*>(take(trows * H / 16));
     w.hq_codes = reinterpret_cast<uint8_t*>(take(trows * I / 2));
@@ -138,6 +144,31 @@ MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
   }
   w.bytes = off;
   return w;
+}
+
+// The routed rows of the layer input in tile-major NVFP4 (the W4A4 gate/up
+// GEMM's A operand), copied from the tokens' rows quantised once: one warp
+// per row r = 128 t + i of tile t; rows i < tile_rows[t] get their token's
+// codes (K/2 bytes) and block scales (re-laid into the MMA layout, four
+// scale columns per 32-bit store), the rest of the tile zeros.
+__global__ void __launch_bounds__(8 * 32) gather_routed_kernel(const uint8_t* codes_in, const uint8_t* scales_in,
+                                                               int64_t K, const int* row_of, const int* tile_count,
+                                                               const int* tile_row0, const int* tile_rows,
+                                                               uint8_t* codes, uint8_t* scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int t = static_cast<int>(r >> 7), i = static_cast<int>(r & 127);
+  if (t >= *tile_count) return;
+  int tok = -1;
+  if (i < tile_rows[t]) tok = row_of[static_cast<int64_t>(tile_row0[t]) + i];
+  const int64_t kb = K / 2, ng = K / 64;   // 16-byte code pieces: kb / 16; scale groups of four: ng
+  const uint4* src = reinterpret_cast<const uint4*>(codes_in + static_cast<int64_t>(tok < 0 ? 0 : tok) * kb);
+  uint4* dst = reinterpret_cast<uint4*>(codes + r * kb);
+  for (int64_t q = lane; q < kb / 16; q += 32) dst[q] = tok >= 0 ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(scales_in + static_cast<int64_t>(tok < 0 ? 0 : tok) * (K / 16));
+  const int64_t srow_off = (r >> 7) * ng * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+  for (int64_t g = lane; g < ng; g += 32)
+    *reinterpret_cast<uint32_t*>(scales + srow_off + g * 512) = tok >= 0 ? __ldg(ssrc + g) : 0u;
 }
 
 // NVFP4 of the routed rows in tile-major order (the W4A4 expert GEMMs' A
@@ -209,7 +240,15 @@ constexpr int XT_MIN_ROWS_PER_EXPERT = 32;
 // Replaces a memset and three kernels (count, plan, scatter). A routed slot
 // whose expert id lies outside [0, E) gets no row (pos_of = -1, so it
 // contributes nothing) and sets NVFP4_ERR_INVALID_ARG in the status word.
+//
+// With PRIVATE (E <= PLAN_PRIVATE_MAX_E) every warp counts into its own
+// histogram in dynamic shared memory (many routed rows share few experts, so
+// one shared counter per expert serialised the atomics of all 1024 threads);
+// each warp's histogram then becomes its exclusive offset within the expert,
+// and in the position pass the warp hands out positions from there.
 constexpr int PLAN_THREADS = 1024;
+constexpr int PLAN_PRIVATE_MAX_E = 256;
+template <bool PRIVATE>
 __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t* ids, int64_t R, int topk, int E,
                                                                   int* poff, int* chunk_count, int* chunk_expert,
                                                                   int* chunk_rows, int* tile_count, int* tile_expert,
@@ -219,8 +258,13 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
   __shared__ int s_off[PLAN_MAX_E];
   __shared__ int s_wr[PLAN_THREADS / 32], s_wt[PLAN_THREADS / 32];
   __shared__ int s_total;
+  extern __shared__ int s_hist[];   // PRIVATE: [PLAN_THREADS / 32][E]
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  for (int e = tid; e < E; e += PLAN_THREADS) s_cnt[e] = 0;
+  if (PRIVATE) {
+    for (int k = tid; k < (PLAN_THREADS / 32) * E; k += PLAN_THREADS) s_hist[k] = 0;
+  } else {
+    for (int e = tid; e < E; e += PLAN_THREADS) s_cnt[e] = 0;
+  }
   __syncthreads();
   for (int64_t i0 = tid; i0 < R; i0 += 4 * PLAN_THREADS) {
     int ev[4];
@@ -231,9 +275,21 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      if (ev[u] >= 0 && ev[u] < E) atomicAdd(&s_cnt[ev[u]], 1);
+      if (ev[u] >= 0 && ev[u] < E) atomicAdd(PRIVATE ? &s_hist[wid * E + ev[u]] : &s_cnt[ev[u]], 1);
   }
   __syncthreads();
+  if (PRIVATE) {
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+      int run = 0;
+      for (int w = 0; w < PLAN_THREADS / 32; ++w) {
+        const int c = s_hist[w * E + e];
+        s_hist[w * E + e] = run;
+        run += c;
+      }
+      s_cnt[e] = run;
+    }
+    __syncthreads();
+  }
   // block scan: thread tid owns experts [tid * ept, tid * ept + ept)
   const int ept = (E + PLAN_THREADS - 1) / PLAN_THREADS;
   int lr = 0, lt = 0;
@@ -289,8 +345,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
   }
   __syncthreads();
   for (int r = tid; r < s_total; r += PLAN_THREADS) row_of[r] = -1;
-  for (int e = tid; e < E; e += PLAN_THREADS) s_cnt[e] = 0;
-  __syncthreads();   // row_of = -1 before any position is written; counts reused as cursors
+  if (!PRIVATE)
+    for (int e = tid; e < E; e += PLAN_THREADS) s_cnt[e] = 0;
+  __syncthreads();   // row_of = -1 before any position is written; counts (or warp offsets) as cursors
   for (int64_t i0 = tid; i0 < R; i0 += 4 * PLAN_THREADS) {
     int ev[4];
 #pragma unroll
@@ -307,11 +364,29 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
         atomicExch(status, NVFP4_ERR_INVALID_ARG);
         continue;
       }
-      const int pos = s_off[ev[u]] + atomicAdd(&s_cnt[ev[u]], 1);
+      const int pos = s_off[ev[u]] + atomicAdd(PRIVATE ? &s_hist[wid * E + ev[u]] : &s_cnt[ev[u]], 1);
       row_of[pos] = static_cast<int>(i / topk);
       pos_of[i] = pos;
     }
   }
+}
+
+int launch_route_plan(const int32_t* ids, int64_t R, int topk, int64_t E, const MoeWs& m, cudaStream_t stream) {
+  if (E <= PLAN_PRIVATE_MAX_E) {
+    const int smem = static_cast<int>((PLAN_THREADS / 32) * E * sizeof(int));
+    const int rc = ensure_smem(route_plan_kernel<true>, smem);
+    if (rc != NVFP4_OK) return rc;
+    route_plan_kernel<true><<<1, PLAN_THREADS, smem, stream>>>(ids, R, topk, static_cast<int>(E), m.poff,
+                                                               m.chunk_count, m.chunk_expert, m.chunk_rows,
+                                                               m.tile_count, m.tile_expert, m.tile_row0, m.tile_rows,
+                                                               m.row_of, m.pos_of, device_status_ptr());
+  } else {
+    route_plan_kernel<false><<<1, PLAN_THREADS, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff,
+                                                             m.chunk_count, m.chunk_expert, m.chunk_rows,
+                                                             m.tile_count, m.tile_expert, m.tile_row0, m.tile_rows,
+                                                             m.row_of, m.pos_of, device_status_ptr());
+  }
+  return from_cuda(cudaGetLastError());
 }
 
 // One CTA per padded row (rows longer than MOE_PREP_MAX_K).
@@ -432,9 +507,10 @@ __global__ void __launch_bounds__(MOE_PREP_WARPS * 32) xprep_moe_rows_kernel(con
   }
 }
 
-// out[t][c] = bf16(sum_j w[t][j] * y[pos(t, j)][c]), slots in order; one
-// thread per 4 columns (H % 4 == 0), CTA (t, column block of 1024).
-__global__ void combine_kernel(const float* ybuf, const int* pos_of, const float* w, int64_t T, int topk,
+// out[t][c] = bf16(sum_j w[t][j] * y[pos(t, j)][c]) in fp32, slots in order
+// (y: the bf16 expert outputs); one thread per 4 columns (H % 4 == 0), CTA
+// (t, column block of 1024).
+__global__ void combine_kernel(const uint16_t* ybuf, const int* pos_of, const float* w, int64_t T, int topk,
                                int64_t H, uint16_t* out) {
   const int64_t t = blockIdx.x;
   const int64_t c = (static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x) * 4;
@@ -444,11 +520,11 @@ __global__ void combine_kernel(const float* ybuf, const int* pos_of, const float
     const int pos = pos_of[t * topk + j];
     if (pos < 0) continue;
     const float wj = w[t * topk + j];
-    const float4 y = *reinterpret_cast<const float4*>(ybuf + static_cast<int64_t>(pos) * H + c);
-    acc.x = fmaf(wj, y.x, acc.x);
-    acc.y = fmaf(wj, y.y, acc.y);
-    acc.z = fmaf(wj, y.z, acc.z);
-    acc.w = fmaf(wj, y.w, acc.w);
+    const uint2 yb = *reinterpret_cast<const uint2*>(ybuf + static_cast<int64_t>(pos) * H + c);
+    acc.x = fmaf(wj, bf16_bits_to_f32(yb.x & 0xFFFFu), acc.x);
+    acc.y = fmaf(wj, bf16_bits_to_f32(yb.x >> 16), acc.y);
+    acc.z = fmaf(wj, bf16_bits_to_f32(yb.y & 0xFFFFu), acc.z);
+    acc.w = fmaf(wj, bf16_bits_to_f32(yb.y >> 16), acc.w);
   }
   uint2 o;
   o.x = f32_to_bf16_bits(acc.x) | (f32_to_bf16_bits(acc.y) << 16);
@@ -567,18 +643,18 @@ int launch_grouped_gemm_w4a4(const uint16_t* X, int64_t T, int topk, const int32
   if (E > PLAN_MAX_E) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   const MoeWs m = carve_moe(ws, T, H, I, E, topk, true);
   if (m.max_tiles * 128 >= (1LL << 31) / (H / 2)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  route_plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.chunk_count,
-                                            m.chunk_expert, m.chunk_rows, m.tile_count, m.tile_expert, m.tile_row0,
-                                            m.tile_rows, m.row_of, m.pos_of, device_status_ptr());
-  int rc = from_cuda(cudaGetLastError());
+  int rc = launch_route_plan(ids, R, topk, E, m, stream);
   if (rc != NVFP4_OK) return rc;
-  rc = launch_amax_bf16(X, T * H, m.amax, stream);
+  // the layer input quantised once per token (dynamic tensor scale), then its
+  // routed rows gathered into the tile-major matrix
+  rc = launch_quantize(X, NVFP4_DTYPE_BF16, T, H, m.xt_codes, m.xt_scales, m.st, NVFP4_ST_COMPUTE,
+                       NVFP4_SCALES_ROWMAJOR, m.q_ws, stream);
   if (rc != NVFP4_OK) return rc;
   if (cudaMemsetAsync(m.amax + 1, 0, sizeof(unsigned int), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
   const int64_t trows = m.max_tiles * 128;
   const unsigned qgrid = static_cast<unsigned>(trows / QR_WARPS);
-  quantize_routed_kernel<<<qgrid, QR_WARPS * 32, 0, stream>>>(X, H, true, m.row_of, m.tile_count, m.tile_row0,
-                                                              m.tile_rows, m.amax, m.st, m.xq_codes, m.xq_scales);
+  gather_routed_kernel<<<qgrid, 8 * 32, 0, stream>>>(m.xt_codes, m.xt_scales, H, m.row_of, m.tile_count, m.tile_row0,
+                                                     m.tile_rows, m.xq_codes, m.xq_scales);
   rc = from_cuda(cudaGetLastError());
   if (rc != NVFP4_OK) return rc;
   rc = launch_grouped_w4a4(true, m.xq_codes, m.xq_scales, m.st, trows, W13, m.tile_count, m.tile_expert, m.tile_row0,
@@ -605,10 +681,7 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
   const int64_t R = T * topk;
   if (E > PLAN_MAX_E) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   const MoeWs m = carve_moe(ws, T, H, I, E, topk);
-  route_plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.chunk_count,
-                                            m.chunk_expert, m.chunk_rows, m.tile_count, m.tile_expert, m.tile_row0,
-                                            m.tile_rows, m.row_of, m.pos_of, device_status_ptr());
-  int rc = from_cuda(cudaGetLastError());
+  int rc = launch_route_plan(ids, R, topk, E, m, stream);
   if (rc != NVFP4_OK) return rc;
 
   // Many rows per expert: the tensor cores (the f16 rows live where the

@@ -25,7 +25,7 @@
 // Gate/up tiles hold 64 gate rows (lanes 0..63) and the matching 64 up rows
 // (lanes 64..127); the epilogue stages both through shared memory, 32 routed
 // rows at a time, and all eight warps write h = bf16(silu(g) * u). Down tiles
-// write fp32 partial outputs per routed row for the combine kernel. The grid
+// write each routed row's expert output (bf16) for the combine kernel. The grid
 // runs the weight blocks of one tile next to each other, so a tile's rows
 // come from DRAM about once.
 // Every mbarrier wait is bounded (device status word + CTA abort flag).
@@ -71,7 +71,7 @@ struct MoeTcParams {
   int inter;               // I
   int hidden;              // H
   uint16_t* h_out;         // gate/up: bf16 [routed rows][I]
-  float* y_out;            // down: fp32 [routed rows][H]
+  uint16_t* y_out;         // down: bf16 [routed rows][H]
   int* status;
 };
 
@@ -281,7 +281,8 @@ __global__ void __launch_bounds__(XT_THREADS, XT_CTAS_PER_SM)
           for (int i = 0; i < 16; ++i) {
             const int t = 32 * j + 16 * half + i;
             if (t < nrows)
-              p.y_out[static_cast<int64_t>(row0 + t) * p.hidden + 128 * wb + r] = __uint_as_float(acc[i]) * mulv[t];
+              p.y_out[static_cast<int64_t>(row0 + t) * p.hidden + 128 * wb + r] =
+                  static_cast<uint16_t>(f32_to_bf16_bits(__uint_as_float(acc[i]) * mulv[t]));
           }
         }
       }
