@@ -50,10 +50,9 @@ NVFP4_DEV uint32_t e2m1x8_of_pairs(uint64_t p0, uint64_t p1, uint64_t p2, uint64
 // where the products with rl and rh give the same codes, those are the codes
 // of the exact quotients. Otherwise (a quotient at or next to a midpoint) the
 // sixteen quotients are formed by IEEE division.
-NVFP4_DEV uint2 e2m1x16(const float (&v)[16], float den) {
-  if (den > 1e-30f && den < 1e30f) {
-    const float r = __frcp_rn(den);
-    const float rh = __fmul_rn(r, 1.0f + 0x1p-20f), rl = __fmul_rn(r, 1.0f - 0x1p-20f);
+// rh, rl are the two brackets of 1 / den (rh = rl = 0: none, divide).
+NVFP4_DEV uint2 e2m1x16_r(const float (&v)[16], float den, float rh, float rl) {
+  if (rh != 0.f) {
     const uint64_t RH = f32_pair(rh, rh), RL = f32_pair(rl, rl);
     uint64_t ph[8], pl[8];
 #pragma unroll
@@ -75,6 +74,63 @@ NVFP4_DEV uint2 e2m1x16(const float (&v)[16], float den) {
   for (int j = 0; j < 8; ++j) q[j] = __fdiv_rn(v[8 + j], den);
   out.y = f32x8_to_e2m1x8(q);
   return out;
+}
+
+// The brackets of 1 / den used by e2m1x16_r: rh > 1 / den > rl (exactly),
+// or zeros when den is too small or too large for them.
+NVFP4_DEV void recip_brackets(float den, float& rh, float& rl) {
+  if (den > 1e-30f && den < 1e30f) {
+    const float r = __frcp_rn(den);
+    rh = __fmul_rn(r, 1.0f + 0x1p-20f);
+    rl = __fmul_rn(r, 1.0f - 0x1p-20f);
+  } else {
+    rh = rl = 0.f;
+  }
+}
+
+NVFP4_DEV uint2 e2m1x16(const float (&v)[16], float den) {
+  float rh, rl;
+  recip_brackets(den, rh, rl);
+  return e2m1x16_r(v, den, rh, rl);
+}
+
+// E4M3 code of fl(ab / d) (ab >= 0): RN(ab rdl) <= fl(ab / d) <= RN(ab rdh)
+// for brackets rdl < 1 / d < rdh (recip_brackets), and the E4M3 rounding is
+// monotone, so equal codes of the two products are the code of the quotient;
+// otherwise (or without brackets) IEEE division.
+NVFP4_DEV uint32_t block_scale_code(float ab, float d, float rdh, float rdl) {
+  if (rdh != 0.f) {
+    const uint32_t h = f32_to_e4m3(__fmul_rn(ab, rdh)), l = f32_to_e4m3(__fmul_rn(ab, rdl));
+    if (h == l) return h;
+  }
+  return f32_to_e4m3(__fdiv_rn(ab, d));
+}
+
+// Per tensor scale, the block step's constants for every E4M3 block-scale
+// code c (0x00 .. 0x7F; 0x7F is never produced): den[c] = fl(e4m3(c) * s_t)
+// and the brackets of 1 / den[c]. Built once per CTA in shared memory, they
+// replace a decode, a multiply and a reciprocal per block.
+struct QuantTables {
+  float den[128];
+  float rh[128];
+  float rl[128];
+};
+
+NVFP4_DEV void quant_tables_init(QuantTables& tb, float st) {
+  for (int c = threadIdx.x; c < 128; c += blockDim.x) {
+    const float den = __fmul_rn(e4m3_to_f32(static_cast<uint32_t>(c)), st);
+    tb.den[c] = den;
+    recip_brackets(den, tb.rh[c], tb.rl[c]);
+  }
+}
+
+// quant_block16 with the block's largest magnitude already known (ab) and the
+// scale-code brackets and tables of the tensor scale: the same decisions.
+NVFP4_DEV uint32_t quant_block16_tab(const float (&v)[16], float ab, float d, float rdh, float rdl,
+                                     const QuantTables& tb, uint2& codes) {
+  const uint32_t sc = block_scale_code(ab, d, rdh, rdl);
+  codes = sc != 0 ? e2m1x16_r(v, tb.den[sc], tb.rh[sc], tb.rl[sc]) : make_uint2(0u, 0u);
+  return sc;
 }
 
 // One block: x[16] (fp32) with tensor scale st and d = fp32(st * 6). Returns

@@ -146,6 +146,27 @@ NVFP4_DEV void unpack16<float>(const uint4 (&w)[4], float (&v)[16]) {
   }
 }
 
+// Largest |x| of a block: bf16 words by packed abs-max (the magnitudes' order
+// is exact in bf16), fp32 values by fmax.
+template <typename T>
+NVFP4_DEV float block_amax(const uint4 (&w)[BlockWords<T>::N], const float (&v)[16]);
+template <>
+NVFP4_DEV float block_amax<uint16_t>(const uint4 (&w)[2], const float (&)[16]) {
+  const uint32_t u[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
+  uint32_t m = u[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(u[i]));
+  // each step takes the magnitudes of both inputs, so m holds max |u| per half
+  return fmaxf(__uint_as_float((m & 0x7FFFu) << 16), __uint_as_float(m & 0x7FFF0000u));
+}
+template <>
+NVFP4_DEV float block_amax<float>(const uint4 (&)[4], const float (&v)[16]) {
+  float ab = 0.f;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) ab = fmaxf(ab, fabsf(v[e]));
+  return ab;
+}
+
 // One thread quantises BPT blocks of 16 elements, 32 blocks apart in the row:
 // the raw words of all of them are requested before any is converted. A warp
 // covers a chunk of 32 * BPT consecutive blocks of a row; warps take chunks
@@ -169,6 +190,7 @@ __global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int6
   constexpr int NW = BlockWords<T>::N;
   constexpr int BPT = 4 / NW;   // 2 blocks (bf16) or 1 (fp32) per thread
   __shared__ unsigned int s_amax;
+  __shared__ QuantTables s_tab;
   // chunk indices fit in 32 bits (checked at launch)
   const uint32_t bpr = static_cast<uint32_t>(K / 16);
   const int cpr = static_cast<int>((bpr + 32 * BPT - 1) / (32 * BPT));
@@ -209,6 +231,10 @@ __global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int6
     st = *s_t;
   }
   const float d = __fmul_rn(st, 6.0f);
+  float rdh, rdl;
+  recip_brackets(d, rdh, rdl);
+  quant_tables_init(s_tab, st);
+  __syncthreads();
   while (row >= 0) {
     const uint32_t b0 = static_cast<uint32_t>(cc) * (32 * BPT) + lane;
     const int64_t srow = LAYOUT == NVFP4_SCALES_MMA
@@ -221,7 +247,7 @@ __global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int6
       float v[16];
       unpack16<T>(raw[u], v);
       uint2 packed;
-      const uint32_t sc = quant_block16(v, st, d, packed);
+      const uint32_t sc = quant_block16_tab(v, block_amax<T>(raw[u], v), d, rdh, rdl, s_tab, packed);
       reinterpret_cast<uint2*>(codes)[static_cast<int64_t>(row) * bpr + bi] = packed;
       scales[LAYOUT == NVFP4_SCALES_MMA ? srow + (bi >> 2) * 512 + (bi & 3) : srow + bi] = static_cast<uint8_t>(sc);
     }
