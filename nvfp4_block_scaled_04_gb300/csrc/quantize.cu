@@ -183,7 +183,7 @@ NVFP4_DEV float block_amax<float>(const uint4 (&)[4], const float (&v)[16]) {
 // pass's programmatic dependent: its first blocks are loaded before it waits
 // for that pass's results.
 template <typename T, int LAYOUT>
-__global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int64_t rows, int64_t K,
+__global__ void __launch_bounds__(Q_THREADS, 4) quantize_kernel(const T* x, int64_t rows, int64_t K,
                                                                  uint8_t* codes, uint8_t* scales,
                                                                  const unsigned int* amax_bits, int n_amax,
                                                                  float* s_t, int mode, int64_t cols4) {
@@ -201,19 +201,30 @@ __global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int6
   int row = c0 >= 0 ? c0 / cpr : -1, cc = c0 >= 0 ? c0 - row * cpr : 0;
   const int drow = warps / cpr, dcc = warps - drow * cpr;
   const int64_t tiles_per_row = cols4 >> 2;
-  uint4 raw[BPT][NW];
-  auto load_chunk = [&]() {
-    const uint32_t b0 = static_cast<uint32_t>(cc) * (32 * BPT) + lane;
-    const T* xrow = x + static_cast<int64_t>(row) * K;
+  // two chunks in flight per warp: the next chunk's words are requested
+  // before the current one is converted
+  uint4 raw[BPT][NW], nxt[BPT][NW];
+  auto load_chunk = [&](int r, int c, uint4 (&dst)[BPT][NW]) {
+    const uint32_t b0 = static_cast<uint32_t>(c) * (32 * BPT) + lane;
+    const T* xrow = x + static_cast<int64_t>(r) * K;
 #pragma unroll
     for (int u = 0; u < BPT; ++u) {
       const uint32_t bi = b0 + 32 * u;
       const uint4* src = reinterpret_cast<const uint4*>(xrow + static_cast<int64_t>(bi < bpr ? bi : 0) * 16);
 #pragma unroll
-      for (int i = 0; i < NW; ++i) raw[u][i] = __ldg(src + i);
+      for (int i = 0; i < NW; ++i) dst[u][i] = __ldg(src + i);
     }
   };
-  if (row >= 0) load_chunk();
+  // the chunk after (row, cc) in this warp's walk
+  auto advance = [&](int& r, int& c) {
+    c -= dcc;
+    r -= drow;
+    if (c < 0) {
+      c += cpr;
+      r -= 1;
+    }
+  };
+  if (row >= 0) load_chunk(row, cc, raw);
   float st;
   if (mode == NVFP4_ST_COMPUTE) {
     pdl_wait();   // the amax pass's maxima are complete and visible
@@ -236,6 +247,9 @@ __global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int6
   quant_tables_init(s_tab, st);
   __syncthreads();
   while (row >= 0) {
+    int nrow = row, ncc = cc;
+    advance(nrow, ncc);
+    if (nrow >= 0) load_chunk(nrow, ncc, nxt);
     const uint32_t b0 = static_cast<uint32_t>(cc) * (32 * BPT) + lane;
     const int64_t srow = LAYOUT == NVFP4_SCALES_MMA
                              ? (static_cast<int64_t>(row >> 7) * tiles_per_row) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4
@@ -251,13 +265,12 @@ __global__ void __launch_bounds__(Q_THREADS, 5) quantize_kernel(const T* x, int6
       reinterpret_cast<uint2*>(codes)[static_cast<int64_t>(row) * bpr + bi] = packed;
       scales[LAYOUT == NVFP4_SCALES_MMA ? srow + (bi >> 2) * 512 + (bi & 3) : srow + bi] = static_cast<uint8_t>(sc);
     }
-    cc -= dcc;
-    row -= drow;
-    if (cc < 0) {
-      cc += cpr;
-      row -= 1;
-    }
-    if (row >= 0) load_chunk();
+    row = nrow;
+    cc = ncc;
+#pragma unroll
+    for (int u = 0; u < BPT; ++u)
+#pragma unroll
+      for (int i = 0; i < NW; ++i) raw[u][i] = nxt[u][i];
   }
 }
 
