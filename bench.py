@@ -446,7 +446,8 @@ def measure_rows(nv, peaks, reps):
     gperm = torch.Generator(device="cuda")
     gperm.manual_seed(6)
     # one 32,768-id mask per draft step, so no step finds its rows still in L2
-    masks = [torch.randperm(V, generator=gperm, device="cuda")[:32768].to(torch.int32) for _ in range(3)]
+    # (six: the steady-state chains below rotate over all of them, 566 MB)
+    masks = [torch.randperm(V, generator=gperm, device="cuda")[:32768].to(torch.int32) for _ in range(6)]
     qmasks = [nv.gather_rows(qh, ix) for ix in masks]   # one-time prepack: masked rows as compact matrices
     head = {}
     for Mh in (1, 4, 8):
@@ -472,9 +473,22 @@ def measure_rows(nv, peaks, reps):
             b = rows * (K // 2 + K // 16) + 2 * Mh * K
             res[label] = {"ms": t, "gbs": b / t / 1e6, "frac_hbm": b / t / 1e6 / peaks["hbm_gbs"]}
         res["full_over_masked_time"] = res["full"]["ms"] / res["masked"]["ms"]
+        # steady state: draft steps chained back to back (12 per graph, the six
+        # compact masks in turn, 566 MB, so no step finds its rows in L2), as a
+        # serving loop runs them between verifications
+        hs6 = [gpu_normal((Mh, K), 1.0, seed=20 + s, dtype=torch.bfloat16) for s in range(6)]
+        ws6 = [torch.zeros(nv.workspace_size(nv.OP_GATHER_ARGMAX, Mh, V, K), dtype=torch.uint8, device="cuda")
+               for _ in range(6)]
+        gs = capture(lambda: [nv.gemv_argmax(hs6[s % 6], qmasks[s % 6], masks[s % 6], workspace=ws6[s % 6])
+                              for s in range(12)])
+        t = time_graph(gs, reps) / 12
+        b = 32768 * (K // 2 + K // 16) + 2 * Mh * K
+        res["masked_steady_state"] = {"ms": t, "gbs": b / t / 1e6, "frac_hbm": b / t / 1e6 / peaks["hbm_gbs"]}
+        del gs
         head[f"M{Mh}"] = res
     head["bytes_ratio_full_over_masked"] = V / 32768
-    head["timing"] = "per draft step: graphs of 3 steps (one mask and hidden state each), L2 flushed per graph"
+    head["timing"] = ("per draft step: graphs of 3 steps (one mask and hidden state each), L2 flushed per graph; "
+                      "masked_steady_state: graphs of 12 chained steps over six masks")
     out["draft_head"] = head
 
     # speculative verify: 8 sequences x (3 drafts + 1) = 32 rows against the
