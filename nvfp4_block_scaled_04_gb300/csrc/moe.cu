@@ -245,10 +245,14 @@ constexpr int XT_MIN_ROWS_PER_EXPERT = 32;
 // histogram in dynamic shared memory (many routed rows share few experts, so
 // one shared counter per expert serialised the atomics of all 1024 threads);
 // each warp's histogram then becomes its exclusive offset within the expert,
-// and in the position pass the warp hands out positions from there.
+// and in the position pass the warp hands out positions from there. With
+// STAGED (R <= PLAN_STAGED_MAX_R) all routed ids are first copied into
+// shared memory with 16-byte loads issued at once, so the two passes over
+// them cost one round trip to memory instead of one per four ids a thread.
 constexpr int PLAN_THREADS = 1024;
 constexpr int PLAN_PRIVATE_MAX_E = 256;
-template <bool PRIVATE>
+constexpr int PLAN_STAGED_MAX_R = 32768;
+template <bool PRIVATE, bool STAGED>
 __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t* ids, int64_t R, int topk, int E,
                                                                   int* poff, int* chunk_count, int* chunk_expert,
                                                                   int* chunk_rows, int* tile_count, int* tile_expert,
@@ -258,8 +262,18 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
   __shared__ int s_off[PLAN_MAX_E];
   __shared__ int s_wr[PLAN_THREADS / 32], s_wt[PLAN_THREADS / 32];
   __shared__ int s_total;
-  extern __shared__ int s_hist[];   // PRIVATE: [PLAN_THREADS / 32][E]
+  extern __shared__ int s_dyn[];    // PRIVATE: [PLAN_THREADS / 32][E] histograms; STAGED: then the R ids
+  int* s_hist = s_dyn;
+  int* s_ids = s_dyn + (PRIVATE ? (PLAN_THREADS / 32) * E : 0);
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (STAGED) {
+    // ids are 16-byte aligned (checked at launch); R4 whole groups of four, then the tail
+    const int64_t r4 = R / 4;
+    for (int64_t q = tid; q < r4; q += PLAN_THREADS)
+      reinterpret_cast<int4*>(s_ids)[q] = __ldg(reinterpret_cast<const int4*>(ids) + q);
+    for (int64_t q = 4 * r4 + tid; q < R; q += PLAN_THREADS) s_ids[q] = ids[q];
+  }
+  auto id_at = [&](int64_t i) { return STAGED ? s_ids[i] : ids[i]; };
   if (PRIVATE) {
     for (int k = tid; k < (PLAN_THREADS / 32) * E; k += PLAN_THREADS) s_hist[k] = 0;
   } else {
@@ -271,7 +285,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int64_t i = i0 + u * PLAN_THREADS;
-      ev[u] = i < R ? ids[i] : -1;
+      ev[u] = i < R ? id_at(i) : -1;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
@@ -353,7 +367,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int64_t i = i0 + u * PLAN_THREADS;
-      ev[u] = i < R ? ids[i] : 0;
+      ev[u] = i < R ? id_at(i) : 0;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -365,28 +379,31 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
         continue;
       }
       const int pos = s_off[ev[u]] + atomicAdd(PRIVATE ? &s_hist[wid * E + ev[u]] : &s_cnt[ev[u]], 1);
-      row_of[pos] = static_cast<int>(i / topk);
+      row_of[pos] = static_cast<int>(static_cast<uint32_t>(i) / static_cast<uint32_t>(topk));
       pos_of[i] = pos;
     }
   }
 }
 
-int launch_route_plan(const int32_t* ids, int64_t R, int topk, int64_t E, const MoeWs& m, cudaStream_t stream) {
-  if (E <= PLAN_PRIVATE_MAX_E) {
-    const int smem = static_cast<int>((PLAN_THREADS / 32) * E * sizeof(int));
-    const int rc = ensure_smem(route_plan_kernel<true>, smem);
-    if (rc != NVFP4_OK) return rc;
-    route_plan_kernel<true><<<1, PLAN_THREADS, smem, stream>>>(ids, R, topk, static_cast<int>(E), m.poff,
-                                                               m.chunk_count, m.chunk_expert, m.chunk_rows,
-                                                               m.tile_count, m.tile_expert, m.tile_row0, m.tile_rows,
-                                                               m.row_of, m.pos_of, device_status_ptr());
-  } else {
-    route_plan_kernel<false><<<1, PLAN_THREADS, 0, stream>>>(ids, R, topk, static_cast<int>(E), m.poff,
-                                                             m.chunk_count, m.chunk_expert, m.chunk_rows,
-                                                             m.tile_count, m.tile_expert, m.tile_row0, m.tile_rows,
-                                                             m.row_of, m.pos_of, device_status_ptr());
-  }
+template <bool PRIVATE, bool STAGED>
+int launch_route_plan_t(const int32_t* ids, int64_t R, int topk, int64_t E, const MoeWs& m, cudaStream_t stream) {
+  const int smem = static_cast<int>(((PRIVATE ? (PLAN_THREADS / 32) * E : 0) + (STAGED ? R : 0)) * sizeof(int));
+  auto k = route_plan_kernel<PRIVATE, STAGED>;
+  const int rc = ensure_smem(k, smem > 0 ? smem : 1);
+  if (rc != NVFP4_OK) return rc;
+  k<<<1, PLAN_THREADS, smem, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.chunk_count, m.chunk_expert,
+                                       m.chunk_rows, m.tile_count, m.tile_expert, m.tile_row0, m.tile_rows, m.row_of,
+                                       m.pos_of, device_status_ptr());
   return from_cuda(cudaGetLastError());
+}
+
+int launch_route_plan(const int32_t* ids, int64_t R, int topk, int64_t E, const MoeWs& m, cudaStream_t stream) {
+  const bool priv = E <= PLAN_PRIVATE_MAX_E;
+  const bool staged = R <= PLAN_STAGED_MAX_R && (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
+  if (priv && staged) return launch_route_plan_t<true, true>(ids, R, topk, E, m, stream);
+  if (priv) return launch_route_plan_t<true, false>(ids, R, topk, E, m, stream);
+  if (staged) return launch_route_plan_t<false, true>(ids, R, topk, E, m, stream);
+  return launch_route_plan_t<false, false>(ids, R, topk, E, m, stream);
 }
 
 // One CTA per padded row (rows longer than MOE_PREP_MAX_K).
@@ -640,7 +657,7 @@ int launch_grouped_gemm_w4a4(const uint16_t* X, int64_t T, int topk, const int32
   if (T == 0) return NVFP4_OK;
   const int64_t E = W13.batch, I = W13.rows / 2, H = W13.K;
   const int64_t R = T * topk;
-  if (E > PLAN_MAX_E) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (E > PLAN_MAX_E || R >= (1LL << 31)) return NVFP4_ERR_UNSUPPORTED_SHAPE;   // plan positions are int
   const MoeWs m = carve_moe(ws, T, H, I, E, topk, true);
   if (m.max_tiles * 128 >= (1LL << 31) / (H / 2)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   int rc = launch_route_plan(ids, R, topk, E, m, stream);
@@ -679,7 +696,7 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
   if (T == 0) return NVFP4_OK;
   const int64_t E = W13.batch, I = W13.rows / 2, H = W13.K;
   const int64_t R = T * topk;
-  if (E > PLAN_MAX_E) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (E > PLAN_MAX_E || R >= (1LL << 31)) return NVFP4_ERR_UNSUPPORTED_SHAPE;   // plan positions are int
   const MoeWs m = carve_moe(ws, T, H, I, E, topk);
   int rc = launch_route_plan(ids, R, topk, E, m, stream);
   if (rc != NVFP4_OK) return rc;
