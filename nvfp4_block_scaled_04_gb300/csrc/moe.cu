@@ -246,13 +246,14 @@ constexpr int XT_MIN_ROWS_PER_EXPERT = 32;
 // one shared counter per expert serialised the atomics of all 1024 threads);
 // each warp's histogram then becomes its exclusive offset within the expert,
 // and in the position pass the warp hands out positions from there. With
-// STAGED (R <= PLAN_STAGED_MAX_R) all routed ids are first copied into
-// shared memory with 16-byte loads issued at once, so the two passes over
-// them cost one round trip to memory instead of one per four ids a thread.
+// SMEM_ROWS (R + 32 E <= PLAN_SMEM_ROWS_MAX) the padded rows' token ids
+// (row_of) are assembled in shared memory and written out with coalesced
+// stores: tens of thousands of scattered 4-byte stores from one SM took
+// longer than the rest of the plan together.
 constexpr int PLAN_THREADS = 1024;
 constexpr int PLAN_PRIVATE_MAX_E = 256;
-constexpr int PLAN_STAGED_MAX_R = 32768;
-template <bool PRIVATE, bool STAGED>
+constexpr int PLAN_SMEM_ROWS_MAX = 40960;
+template <bool PRIVATE, bool SMEM_ROWS>
 __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t* ids, int64_t R, int topk, int E,
                                                                   int* poff, int* chunk_count, int* chunk_expert,
                                                                   int* chunk_rows, int* tile_count, int* tile_expert,
@@ -262,18 +263,12 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
   __shared__ int s_off[PLAN_MAX_E];
   __shared__ int s_wr[PLAN_THREADS / 32], s_wt[PLAN_THREADS / 32];
   __shared__ int s_total;
-  extern __shared__ int s_dyn[];    // PRIVATE: [PLAN_THREADS / 32][E] histograms; STAGED: then the R ids
+  extern __shared__ int s_dyn[];    // PRIVATE: [PLAN_THREADS / 32][E] histograms; SMEM_ROWS: then row_of
   int* s_hist = s_dyn;
-  int* s_ids = s_dyn + (PRIVATE ? (PLAN_THREADS / 32) * E : 0);
+  int* s_rows = s_dyn + (PRIVATE ? (PLAN_THREADS / 32) * E : 0);
+  int* rows_out = SMEM_ROWS ? s_rows : row_of;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (STAGED) {
-    // ids are 16-byte aligned (checked at launch); R4 whole groups of four, then the tail
-    const int64_t r4 = R / 4;
-    for (int64_t q = tid; q < r4; q += PLAN_THREADS)
-      reinterpret_cast<int4*>(s_ids)[q] = __ldg(reinterpret_cast<const int4*>(ids) + q);
-    for (int64_t q = 4 * r4 + tid; q < R; q += PLAN_THREADS) s_ids[q] = ids[q];
-  }
-  auto id_at = [&](int64_t i) { return STAGED ? s_ids[i] : ids[i]; };
+  auto id_at = [&](int64_t i) { return ids[i]; };
   if (PRIVATE) {
     for (int k = tid; k < (PLAN_THREADS / 32) * E; k += PLAN_THREADS) s_hist[k] = 0;
   } else {
@@ -358,7 +353,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
     *tile_count = tiles;
   }
   __syncthreads();
-  for (int r = tid; r < s_total; r += PLAN_THREADS) row_of[r] = -1;
+  for (int r = tid; r < s_total; r += PLAN_THREADS) rows_out[r] = -1;
   if (!PRIVATE)
     for (int e = tid; e < E; e += PLAN_THREADS) s_cnt[e] = 0;
   __syncthreads();   // row_of = -1 before any position is written; counts (or warp offsets) as cursors
@@ -379,16 +374,22 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
         continue;
       }
       const int pos = s_off[ev[u]] + atomicAdd(PRIVATE ? &s_hist[wid * E + ev[u]] : &s_cnt[ev[u]], 1);
-      row_of[pos] = static_cast<int>(static_cast<uint32_t>(i) / static_cast<uint32_t>(topk));
+      rows_out[pos] = static_cast<int>(static_cast<uint32_t>(i) / static_cast<uint32_t>(topk));
       pos_of[i] = pos;
     }
   }
+  if (SMEM_ROWS) {
+    __syncthreads();
+    for (int r = tid; r < s_total; r += PLAN_THREADS) row_of[r] = s_rows[r];
+  }
 }
 
-template <bool PRIVATE, bool STAGED>
+template <bool PRIVATE, bool SMEM_ROWS>
 int launch_route_plan_t(const int32_t* ids, int64_t R, int topk, int64_t E, const MoeWs& m, cudaStream_t stream) {
-  const int smem = static_cast<int>(((PRIVATE ? (PLAN_THREADS / 32) * E : 0) + (STAGED ? R : 0)) * sizeof(int));
-  auto k = route_plan_kernel<PRIVATE, STAGED>;
+  const int64_t rows_max = R + GV_MCHUNK * E;   // the padded rows never exceed this
+  const int smem =
+      static_cast<int>(((PRIVATE ? (PLAN_THREADS / 32) * E : 0) + (SMEM_ROWS ? rows_max : 0)) * sizeof(int));
+  auto k = route_plan_kernel<PRIVATE, SMEM_ROWS>;
   const int rc = ensure_smem(k, smem > 0 ? smem : 1);
   if (rc != NVFP4_OK) return rc;
   k<<<1, PLAN_THREADS, smem, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.chunk_count, m.chunk_expert,
@@ -399,7 +400,7 @@ int launch_route_plan_t(const int32_t* ids, int64_t R, int topk, int64_t E, cons
 
 int launch_route_plan(const int32_t* ids, int64_t R, int topk, int64_t E, const MoeWs& m, cudaStream_t stream) {
   const bool priv = E <= PLAN_PRIVATE_MAX_E;
-  const bool staged = R <= PLAN_STAGED_MAX_R && (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
+  const bool staged = R + GV_MCHUNK * E <= PLAN_SMEM_ROWS_MAX;
   if (priv && staged) return launch_route_plan_t<true, true>(ids, R, topk, E, m, stream);
   if (priv) return launch_route_plan_t<true, false>(ids, R, topk, E, m, stream);
   if (staged) return launch_route_plan_t<false, true>(ids, R, topk, E, m, stream);
