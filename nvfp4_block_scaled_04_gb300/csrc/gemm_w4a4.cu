@@ -469,40 +469,9 @@ constexpr int P_BAND = 16;                                             // m-pair
 // kind::mxf4nvf4, E2M1 x E2M1, K-major, N = 256, M = 256 (the pair)
 constexpr uint32_t P_IDESC = (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(256 >> 4) << 24);
 
-NVFP4_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Bounded wait on a barrier that threads of the peer CTA arrive on.
 NVFP4_DEV bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t n = 0;; ++n) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((n & 63) == 63) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-        atomicExch(&g_device_status, NVFP4_ERR_TIMEOUT);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
-// Arrive on the barrier at the same shared-memory offset in CTA `rank` of the cluster.
-NVFP4_DEV void mbar_arrive_cluster(uint32_t bar, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(rank));
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+  return mbar_wait_cluster_bounded(bar, parity, abort_flag, &g_device_status);
 }
 
 NVFP4_DEV void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa, uint32_t sfb,
@@ -513,15 +482,6 @@ NVFP4_DEV void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint
       "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %6, [%3], [%4], p;\n\t}" ::"r"(
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(sfa), "r"(sfb), "r"(accumulate), "r"(P_IDESC)
-      : "memory");
-}
-
-// Arrive once on the barrier at this offset in both CTAs of the pair when the
-// MMAs issued so far have completed.
-NVFP4_DEV void tc_commit_pair(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(static_cast<uint16_t>(3))
       : "memory");
 }
 

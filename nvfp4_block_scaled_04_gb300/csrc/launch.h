@@ -62,6 +62,10 @@ int ensure_smem(Kernel kernel, int bytes) {
 // ---- tma_host.cu: 2-D uint8 tensor map (inner dimension contiguous).
 int make_tmap_2d_u8(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t row_stride,
                     int box_inner, int box_outer, int swizzle);
+// 3-D uint8 tensor map: dimension 0 contiguous, dimensions 1 and 2 at the
+// given byte strides (which may overlap: dimension 2 can step inside 1).
+int make_tmap_3d_u8(CUtensorMap* map, const void* base, int64_t d0, int64_t d1, int64_t d2, int64_t stride1,
+                    int64_t stride2, int box0, int box1, int box2, int swizzle);
 // 2-D 16-bit map (e.g. a bf16 output), rows of row_stride_bytes.
 int make_tmap_2d_u16(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t row_stride_bytes,
                      int box_inner, int box_outer, int swizzle);

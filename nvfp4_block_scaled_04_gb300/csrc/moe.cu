@@ -64,12 +64,18 @@ __global__ void route_kernel(const float* logits, int64_t T, int E, int topk, in
   }
 }
 
+// tile sizes of the routing plan: the W4A4 expert GEMM takes tiles of up to
+// 128 routed rows (its MMAs are M = 128 over routed rows), the W4A16
+// tensor-core kernel tiles of up to XT_NMAX; the tile table is sized for the
+// smaller
+constexpr int PLAN_TILE_MIN = 128;
+
 struct MoeWs {
   int* chunk_count;   // [1]
   int* poff;          // [E]
   int* chunk_expert;  // [max_chunks]
   int* chunk_rows;    // [max_chunks]
-  int* tile_count;    // [1]  tensor-core tiles: up to XT_NMAX rows of one expert
+  int* tile_count;    // [1]  tensor-core tiles: up to tile_max rows of one expert, split evenly
   int* tile_expert;   // [max_tiles]
   int* tile_row0;     // [max_tiles]
   int* tile_rows;     // [max_tiles]
@@ -103,7 +109,7 @@ MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
   MoeWs w{};
   const int64_t R = T * topk;
   w.max_chunks = ceil_div(R, GV_MCHUNK) + E;
-  w.max_tiles = ceil_div(R, XT_NMAX) + E;
+  w.max_tiles = ceil_div(R, PLAN_TILE_MIN) + E;
   const int64_t rows = w.max_chunks * GV_MCHUNK;
   char* b = static_cast<char*>(base);
   size_t off = 0;
@@ -234,7 +240,7 @@ constexpr int XT_MIN_ROWS_PER_EXPERT = 32;
 // The whole routing plan in one CTA: count the routed rows per expert (shared
 // atomics, four id loads in flight per thread), pad each expert to a multiple
 // of 32 rows and take the exclusive prefix sums of the padded rows and of the
-// tensor-core tiles (each expert's rows in tiles of up to XT_NMAX) with a
+// tensor-core tiles (each expert's rows in tiles of up to tile_max) with a
 // block scan, write the chunk and tile tables and row_of = -1, then hand out
 // each routed row's position within its expert (shared atomics again).
 // Replaces a memset and three kernels (count, plan, scatter). A routed slot
@@ -258,7 +264,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
                                                                   int* poff, int* chunk_count, int* chunk_expert,
                                                                   int* chunk_rows, int* tile_count, int* tile_expert,
                                                                   int* tile_row0, int* tile_rows, int* row_of,
-                                                                  int* pos_of, int* status) {
+                                                                  int* pos_of, int* status, int tile_max) {
   __shared__ int s_cnt[PLAN_MAX_E];
   __shared__ int s_off[PLAN_MAX_E];
   __shared__ int s_wr[PLAN_THREADS / 32], s_wt[PLAN_THREADS / 32];
@@ -306,7 +312,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
     const int e = tid * ept + j;
     if (e < E) {
       lr += (s_cnt[e] + GV_MCHUNK - 1) / GV_MCHUNK * GV_MCHUNK;
-      lt += (s_cnt[e] + XT_NMAX - 1) / XT_NMAX;
+      lt += (s_cnt[e] + tile_max - 1) / tile_max;
     }
   }
   int ir = lr, it = lt;   // inclusive within the warp
@@ -335,10 +341,14 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
       const int n = s_cnt[e];
       s_off[e] = acc;
       poff[e] = acc;
-      for (int r = 0; r < n; r += XT_NMAX, ++tiles) {
+      // as many tiles as tile_max needs, of equal size rounded up to 32 rows
+      // (at most tile_max, so there are exactly that many)
+      const int nt = (n + tile_max - 1) / tile_max;
+      const int sz = nt > 0 ? ((n + nt - 1) / nt + 31) / 32 * 32 : tile_max;
+      for (int r = 0; r < n; r += sz, ++tiles) {
         tile_expert[tiles] = e;
         tile_row0[tiles] = acc + r;
-        tile_rows[tiles] = min(XT_NMAX, n - r);
+        tile_rows[tiles] = min(sz, n - r);
       }
       for (int c = 0; c * GV_MCHUNK < n; ++c) {
         chunk_expert[acc / GV_MCHUNK + c] = e;
@@ -385,7 +395,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
 }
 
 template <bool PRIVATE, bool SMEM_ROWS>
-int launch_route_plan_t(const int32_t* ids, int64_t R, int topk, int64_t E, const MoeWs& m, cudaStream_t stream) {
+int launch_route_plan_t(const int32_t* ids, int64_t R, int topk, int64_t E, const MoeWs& m, int tile_max,
+                        cudaStream_t stream) {
   const int64_t rows_max = R + GV_MCHUNK * E;   // the padded rows never exceed this
   const int smem =
       static_cast<int>(((PRIVATE ? (PLAN_THREADS / 32) * E : 0) + (SMEM_ROWS ? rows_max : 0)) * sizeof(int));
@@ -394,17 +405,19 @@ int launch_route_plan_t(const int32_t* ids, int64_t R, int topk, int64_t E, cons
   if (rc != NVFP4_OK) return rc;
   k<<<1, PLAN_THREADS, smem, stream>>>(ids, R, topk, static_cast<int>(E), m.poff, m.chunk_count, m.chunk_expert,
                                        m.chunk_rows, m.tile_count, m.tile_expert, m.tile_row0, m.tile_rows, m.row_of,
-                                       m.pos_of, device_status_ptr());
+                                       m.pos_of, device_status_ptr(), tile_max);
   return from_cuda(cudaGetLastError());
 }
 
-int launch_route_plan(const int32_t* ids, int64_t R, int topk, int64_t E, const MoeWs& m, cudaStream_t stream) {
+// tile_max: a multiple of 32, at least PLAN_TILE_MIN
+int launch_route_plan(const int32_t* ids, int64_t R, int topk, int64_t E, const MoeWs& m, int tile_max,
+                      cudaStream_t stream) {
   const bool priv = E <= PLAN_PRIVATE_MAX_E;
   const bool staged = R + GV_MCHUNK * E <= PLAN_SMEM_ROWS_MAX;
-  if (priv && staged) return launch_route_plan_t<true, true>(ids, R, topk, E, m, stream);
-  if (priv) return launch_route_plan_t<true, false>(ids, R, topk, E, m, stream);
-  if (staged) return launch_route_plan_t<false, true>(ids, R, topk, E, m, stream);
-  return launch_route_plan_t<false, false>(ids, R, topk, E, m, stream);
+  if (priv && staged) return launch_route_plan_t<true, true>(ids, R, topk, E, m, tile_max, stream);
+  if (priv) return launch_route_plan_t<true, false>(ids, R, topk, E, m, tile_max, stream);
+  if (staged) return launch_route_plan_t<false, true>(ids, R, topk, E, m, tile_max, stream);
+  return launch_route_plan_t<false, false>(ids, R, topk, E, m, tile_max, stream);
 }
 
 // One CTA per padded row (rows longer than MOE_PREP_MAX_K).
@@ -600,25 +613,38 @@ int prep_moe_rows(const uint16_t* src, int64_t K, bool gather, const MoeWs& m, v
   return from_cuda(cudaGetLastError());
 }
 
-// One expert GEMM on the tensor cores: CTA (tile, weight block), CTAs past
-// the routed tiles exit at once. xrow holds the f16 rows [padded rows][K].
+// One expert GEMM on the tensor cores: a persistent kernel, one CTA pair per
+// two SMs walking the (tile, weight-block pair) items that the routing plan
+// produced. xrow holds the f16 rows [padded rows][K].
 template <bool GATEUP>
 int launch_moe_tc(const nvfp4_tensor_t& W, const MoeWs& m, const void* xrow, const MoeTcParams& p,
                   cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(W.batch) * W.rows;
   const int64_t prow = m.max_chunks * GV_MCHUNK;
   CUtensorMap mx, mw;
-  int rc = make_tmap_2d_u16(&mx, xrow, p.K, prow, static_cast<int64_t>(p.K) * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  int rc = make_tmap_2d_u16(&mx, xrow, p.K, prow, static_cast<int64_t>(p.K) * 2, 64, XT_NMAX / 2,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != NVFP4_OK) return rc;
-  rc = make_tmap_2d_u8(&mw, W.codes, W.K / 2, rows, W.K / 2, 32, GATEUP ? 64 : 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+  // codes in 64-byte rows (128 K), 64B swizzle; gate/up: 64 gate rows and
+  // the 64 up rows I further on in one box
+  rc = GATEUP ? make_tmap_3d_u8(&mw, W.codes, W.K / 2, rows, 2, W.K / 2, static_cast<int64_t>(p.inter) * (W.K / 2), 64,
+                                64, 2, CU_TENSOR_MAP_SWIZZLE_64B)
+              : make_tmap_2d_u8(&mw, W.codes, W.K / 2, rows, W.K / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (rc != NVFP4_OK) return rc;
+  // the output: gate/up h [rows][I], boxes of 16 columns; down y [rows][H], 32 columns
+  CUtensorMap mo;
+  rc = GATEUP ? make_tmap_2d_u16(&mo, p.h_out, p.inter, prow, static_cast<int64_t>(p.inter) * 2, 16, 32,
+                                 CU_TENSOR_MAP_SWIZZLE_NONE)
+              : make_tmap_2d_u16(&mo, p.y_out, p.hidden, prow, static_cast<int64_t>(p.hidden) * 2, 32, 32,
+                                 CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc != NVFP4_OK) return rc;
   auto k = moe_tc_kernel<GATEUP>;
   rc = ensure_smem(k, XT_SMEM);
   if (rc != NVFP4_OK) return rc;
-  const unsigned blocks = static_cast<unsigned>(GATEUP ? p.inter / 64 : p.hidden / 128);
-  // weight blocks along x: the CTAs of one routed-row tile run next to each other
-  return launch_ex(k, dim3(blocks, static_cast<unsigned>(m.max_tiles)), dim3(XT_THREADS), XT_SMEM, 1, false, stream,
-                   mx, mw, p);
+  const int64_t work_max = m.max_tiles * (GATEUP ? p.inter / 64 : p.hidden / 128) / 2;
+  const int64_t pairs_max = sm_count() / 2;
+  const unsigned grid = static_cast<unsigned>(2 * (work_max < pairs_max ? work_max : pairs_max));
+  return launch_ex(k, dim3(grid), dim3(XT_THREADS), XT_SMEM, 2, false, stream, mx, mw, mo, p);
 }
 
 int combine(const MoeWs& m, const float* w, int64_t T, int topk, int64_t H, uint16_t* out, cudaStream_t stream) {
@@ -661,7 +687,7 @@ int launch_grouped_gemm_w4a4(const uint16_t* X, int64_t T, int topk, const int32
   if (E > PLAN_MAX_E || R >= (1LL << 31)) return NVFP4_ERR_UNSUPPORTED_SHAPE;   // plan positions are int
   const MoeWs m = carve_moe(ws, T, H, I, E, topk, true);
   if (m.max_tiles * 128 >= (1LL << 31) / (H / 2)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  int rc = launch_route_plan(ids, R, topk, E, m, stream);
+  int rc = launch_route_plan(ids, R, topk, E, m, PLAN_TILE_MIN, stream);
   if (rc != NVFP4_OK) return rc;
   // the layer input quantised once per token (dynamic tensor scale), then its
   // routed rows gathered into the tile-major matrix
@@ -699,13 +725,13 @@ int launch_grouped_gemm(const uint16_t* X, int64_t T, int topk, const int32_t* i
   const int64_t R = T * topk;
   if (E > PLAN_MAX_E || R >= (1LL << 31)) return NVFP4_ERR_UNSUPPORTED_SHAPE;   // plan positions are int
   const MoeWs m = carve_moe(ws, T, H, I, E, topk);
-  int rc = launch_route_plan(ids, R, topk, E, m, stream);
+  int rc = launch_route_plan(ids, R, topk, E, m, XT_NMAX, stream);
   if (rc != NVFP4_OK) return rc;
 
   // Many rows per expert: the tensor cores (the f16 rows live where the
   // fragment-order copies would).
   if (R >= XT_MIN_ROWS_PER_EXPERT * E && m.max_tiles <= 65535 && H % 256 == 0 && I % 256 == 0 && H <= MOE_PREP_MAX_K &&
-      I <= MOE_PREP_MAX_K && ((reinterpret_cast<uintptr_t>(W13.scales) | reinterpret_cast<uintptr_t>(W2.scales)) & 3) == 0) {
+      I <= MOE_PREP_MAX_K && ((reinterpret_cast<uintptr_t>(W13.scales) | reinterpret_cast<uintptr_t>(W2.scales)) & 15) == 0) {
     rc = prep_moe_rows(X, H, true, m, m.xfrag1, m.pexp1, stream);
     if (rc != NVFP4_OK) return rc;
     MoeTcParams p{};

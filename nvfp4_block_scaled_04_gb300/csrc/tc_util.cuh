@@ -54,6 +54,54 @@ NVFP4_DEV bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* ab
   }
 }
 
+// ---- barriers that threads or the tensor cores of the other CTA of a
+// cluster arrive on (CTA pairs)
+
+NVFP4_DEV bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait (cluster-scope acquire), with the give-up rules of mbar_wait_bounded.
+NVFP4_DEV bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 0;; ++n) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((n & 63) == 63) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+        if (status) atomicExch(status, NVFP4_ERR_TIMEOUT);
+        if (abort_flag) *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Arrive on the barrier at the same shared-memory offset in CTA `rank` of the cluster.
+NVFP4_DEV void mbar_arrive_cluster(uint32_t bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(rank));
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+// Arrive once on the barrier at this offset in both CTAs of the pair when the
+// tensor-core operations this thread issued so far have completed.
+NVFP4_DEV void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
 NVFP4_DEV void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -67,6 +115,14 @@ NVFP4_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           dst),
       "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+NVFP4_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 

@@ -38,6 +38,20 @@ int make_tmap_2d_u8(CUtensorMap* map, const void* base, int64_t inner, int64_t o
   return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+int make_tmap_3d_u8(CUtensorMap* map, const void* base, int64_t d0, int64_t d1, int64_t d2, int64_t stride1,
+                    int64_t stride2, int box0, int box1, int box2, int swizzle) {
+  auto encode = get_encode();
+  if (!encode) return NVFP4_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d0), static_cast<cuuint64_t>(d1), static_cast<cuuint64_t>(d2)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(stride1), static_cast<cuuint64_t>(stride2)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box0), static_cast<cuuint32_t>(box1), static_cast<cuuint32_t>(box2)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, static_cast<CUtensorMapSwizzle>(swizzle),
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 int make_tmap_2d_u16(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t row_stride_bytes,
                      int box_inner, int box_outer, int swizzle) {
   auto encode = get_encode();

@@ -104,10 +104,11 @@ def test_moe_config_t256_sampled_tokens():
 
 
 # With at least 32 routed rows per expert on average (and H, I multiples of
-# 256) the expert GEMMs run on the tensor cores: tiles of up to 128 routed
+# 256) the expert GEMMs run on the tensor cores: tiles of up to 256 routed
 # rows of one expert.
 @pytest.mark.parametrize("T,E,H,I,k", [(512, 8, 256, 256, 2), (300, 4, 256, 256, 1), (1024, 4, 256, 512, 2),
-                                       (700, 16, 512, 256, 3), (128, 8, 256, 256, 2)])
+                                       (700, 16, 512, 256, 3), (128, 8, 256, 256, 2),
+                                       (4096, 4, 256, 256, 2)])
 def test_tensor_core_layers(T, E, H, I, k):
     logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=T + 1)
     ids, wts, oids, ow = oracle_routing(logits.numpy(), k)
@@ -118,7 +119,8 @@ def test_tensor_core_layers(T, E, H, I, k):
 
 
 def test_tensor_core_skewed_routing_ragged_tiles():
-    """600 rows on one expert: four tiles of 128 rows and one of 88; the other experts get none."""
+    """600 rows on one expert: three tiles of 200 rows (the plan splits an expert evenly into
+    tiles of at most 256, rounded up to 32 rows); the other experts get none."""
     T, E, H, I = 600, 4, 256, 256
     logits, x, w13, w2 = moe_case(T, E, H, I, 1, seed=11)
     ids = torch.full((T, 1), 1, dtype=torch.int32, device=DEV)
