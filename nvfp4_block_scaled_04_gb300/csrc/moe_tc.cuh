@@ -28,22 +28,25 @@
 //   warps 0, 26   TMA producers, taking alternate 128-K stages
 //   warp 1        tensor-memory allocation; in the even CTA lane 0 issues
 //                 the MMAs (A from tensor memory)
-//   warps 2..17   dequantise, in two groups of eight that take the first and
+//   warps 2..9    dequantise, in two groups of four that take the first and
 //                 the second 64-K step of each stage: warp w owns tensor-memory
-//                 lanes 32 (w % 4).. and one 32-K half of a step, one weight
-//                 row per thread: codes -> f16 pairs (cvt e2m1x2), times the
-//                 block scale (exact in f16), tcgen05.st into the step's A
-//                 slot (8 slots, step j uses j % 8)
-//   warps 18..25  epilogue: warp w reads tensor-memory lanes 32 (w % 4).. of
-//                 every other 32-column group of the accumulator
+//                 lanes 32 (w % 4).., one weight row per thread: codes -> f16
+//                 pairs (cvt e2m1x2), times the block scale (exact in f16),
+//                 tcgen05.st into the step's A slot (8 slots, step j uses j % 8)
+//   warps 10..25  epilogue: warp w reads tensor-memory lanes 32 (w % 4).. of
+//                 every fourth 32-column group of the accumulator
 // Gate/up blocks interleave their rows: tensor-memory lane 2n holds gate row
 // n of the block and lane 2n + 1 up row n, so one shfl.xor gives each thread
 // both values and h = bf16(silu(g) * u) needs no shared-memory exchange. The
 // accumulator (256 columns) leaves no room for a second one, so the MMAs of
-// the next item wait for the epilogue (measured with wait counters: the MMA
-// thread spent 29% (gate/up) and 48% (down) of its time there while the
-// epilogue wrote 2-byte scattered stores); the epilogue therefore stages each
-// warp's 32 routed rows in shared memory and writes them with one TMA store.
+// the next item wait until every epilogue warp has read its last column group
+// (measured with wait counters: the MMA thread spent 29% (gate/up) and 48%
+// (down) of its time there while the epilogue wrote 2-byte scattered
+// stores). So the epilogue stages each warp's 32 routed rows in shared memory
+// and writes them with one TMA store, and sixteen epilogue warps (each with
+// at most two column groups) release the accumulator after at most one group
+// of work; the dequantising warps were idle two thirds of the time, so eight
+// of them do that work.
 // Down blocks write each routed row's expert output (bf16) for the combine
 // kernel.
 //
@@ -51,11 +54,11 @@
 //   full[s]     this CTA's codes and routed rows of stage s landed
 //   empty[s]    the pair's MMAs have consumed stage s (one multicast commit)
 //   ready[a]    in the even CTA only: both CTAs' dequantising warps have
-//               filled A slot a (16 arrivals, 8 remote)
+//               filled A slot a (8 arrivals, 4 remote)
 //   aempty[a]   the pair's MMAs reading A slot a completed (multicast commit)
 //   accf        the accumulator holds a finished item (one multicast commit)
 //   acce        in the even CTA only: both CTAs' epilogues have read the
-//               accumulator (16 arrivals, 8 remote)
+//               accumulator (32 arrivals, 16 remote)
 // Every wait is bounded (device status word + CTA abort flag), and both CTAs
 // reach the closing cluster barrier on every path, so a CTA never leaves
 // while its peer may still touch its memory.
@@ -78,10 +81,10 @@ constexpr int XT_C_BYTES = 128 * 64;                     // 128 weight rows x 64
 constexpr int XT_STAGE_BYTES = XT_B_BYTES + XT_C_BYTES;  // a multiple of 1024
 constexpr int XT_A_COL0 = XT_NMAX;                       // tensor memory: the accumulator, then the A slots
 constexpr int XT_TMEM_COLS = 512;
-constexpr int XT_DQ_GROUP = 8;                           // warps converting one step in one CTA
+constexpr int XT_DQ_GROUP = 4;                           // warps converting one step in one CTA
 constexpr int XT_DQ_WARPS = 2 * XT_DQ_GROUP;
 constexpr int XT_DQ_WARP0 = 2;
-constexpr int XT_EPI_WARPS = 8;
+constexpr int XT_EPI_WARPS = 16;
 constexpr int XT_EPI_WARP0 = XT_DQ_WARP0 + XT_DQ_WARPS;
 constexpr int XT_PROD1_WARP = XT_EPI_WARP0 + XT_EPI_WARPS;   // the second producer
 constexpr int XT_THREADS = (XT_PROD1_WARP + 1) * 32;
@@ -275,16 +278,14 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
       mbar_wait_cluster_bounded(drain_bar, 0, nullptr, p.status);
     }
   } else if (warp >= XT_DQ_WARP0 && warp < XT_EPI_WARP0) {
-    const int dw = warp - XT_DQ_WARP0;                 // 0..15
+    const int dw = warp - XT_DQ_WARP0;                 // 0..7
     const int grp = dw / XT_DQ_GROUP;                  // the step of each stage this warp converts
     const int quarter = warp & 3;                      // tensor-memory lane quarter
-    const int half = (dw % XT_DQ_GROUP) >> 2;          // which 32 K of a step
     const int r = quarter * 32 + lane;                 // tensor-memory lane
     // its weight row: down r; gate/up gate row r / 2 (r even) or up row r / 2
     // (r odd), which the codes box holds at row r / 2, resp. 64 + r / 2
     const int crow = GATEUP ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;
-    const uint32_t a_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + XT_A_COL0 + 16 * half;
-    const int c16 = 2 * grp + half;                    // 16-byte chunk of the row's 64 code bytes
+    const uint32_t a_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + XT_A_COL0;
     int it0 = 0;                                       // the item's first stage
     bool ok = true;
     for (int w = pair_id; w < n_work && ok; w += n_pairs, it0 += n_st) {
@@ -315,20 +316,25 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
           break;
         }
         const uint32_t sc = (ks & 1) == 0 ? (grp ? sc_cur.y : sc_cur.x) : (grp ? sc_cur.w : sc_cur.z);
-        const uint32_t s01 = e4m3x2_to_f16x2(half ? (sc >> 16) : (sc & 0xFFFFu));
-        const uint32_t bscale[2] = {dup_lo(s01), dup_hi(s01)};
-        // the row's 16-byte chunk c16 at its 64B-swizzled place
-        const uint4 c = lds128(stage_c(s) + crow * 64 + ((c16 ^ ((crow >> 1) & 3)) << 4));
-        const uint32_t wv[4] = {c.x, c.y, c.z, c.w};
-        uint32_t v[16];
+        // the row's 32 code bytes of this step: 16-byte chunks 2 grp, 2 grp + 1
+        // at their 64B-swizzled places
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint32_t f[4];
-          e2m1x8_to_f16x2(wv[e], f);
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint32_t s01 = e4m3x2_to_f16x2(hf ? (sc >> 16) : (sc & 0xFFFFu));
+          const uint32_t bscale[2] = {dup_lo(s01), dup_hi(s01)};
+          const int c16 = 2 * grp + hf;
+          const uint4 c = lds128(stage_c(s) + crow * 64 + ((c16 ^ ((crow >> 1) & 3)) << 4));
+          const uint32_t wv[4] = {c.x, c.y, c.z, c.w};
+          uint32_t v[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) v[4 * e + i] = hmul2(f[i], bscale[e / 2]);
+          for (int e = 0; e < 4; ++e) {
+            uint32_t f[4];
+            e2m1x8_to_f16x2(wv[e], f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[4 * e + i] = hmul2(f[i], bscale[e / 2]);
+          }
+          tc_st_16cols(a_lane + a * 32 + 16 * hf, v);
         }
-        tc_st_16cols(a_lane + a * 32, v);
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -337,11 +343,11 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
     }
   } else if (warp >= XT_EPI_WARP0 && warp < XT_EPI_WARP0 + XT_EPI_WARPS) {
     // epilogue: every epilogue warp takes part in the named barrier of an
-    // item; a failed wait is agreed on by all eight (bar.red) before any leaves
+    // item; a failed wait is agreed on by all sixteen (bar.red) before any leaves
     const int quarter = warp & 3;
-    const int ew = warp - XT_EPI_WARP0;               // 0..7
-    const int ch = ew >> 2;                           // column groups j with j % 2 == ch
-    const int et = threadIdx.x - XT_EPI_WARP0 * 32;   // 0..255
+    const int ew = warp - XT_EPI_WARP0;               // 0..15
+    const int ch = ew >> 2;                           // column groups j with j % 4 == ch
+    const int et = threadIdx.x - XT_EPI_WARP0 * 32;   // 0..511
     const uint32_t lanes = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t stg = stg_base + static_cast<uint32_t>(ew) * 2 * XT_STG_BYTES;
     // output columns of this warp within the block: gate/up 16 intermediate
@@ -359,11 +365,11 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
       const bool got = __all_sync(0xffffffffu, mbar_wait_cluster_bounded(accf_bar, item & 1, abort_flag, p.status));
       if (!xt_all_epilogue(got && *abort_flag == 0)) break;
       tc_fence_after();
-      for (int j = ch; j < nbox; j += 2, ++nstore) {
+      for (int j = ch; j < nbox; j += 4, ++nstore) {
         uint32_t a[32];
         tc_ld_32cols(tmem + lanes + static_cast<uint32_t>(32 * j), a);
         tc_wait_ld();
-        if (j + 2 >= nbox) {
+        if (j + 4 >= nbox) {
           // the accumulator's last reads of this item: let the MMAs of the next one start
           tc_fence_before();
           __syncwarp();
