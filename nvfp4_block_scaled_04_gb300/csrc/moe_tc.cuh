@@ -32,7 +32,7 @@
 //                 the second 64-K step of each stage: warp w owns tensor-memory
 //                 lanes 32 (w % 4).., one weight row per thread: codes -> f16
 //                 pairs (cvt e2m1x2), times the block scale (exact in f16),
-//                 tcgen05.st into the step's A slot (8 slots, step j uses j % 8)
+//                 tcgen05.st into the step's A slot (stage s, step q: slot 2 s + q)
 //   warps 10..25  epilogue: warp w reads tensor-memory lanes 32 (w % 4).. of
 //                 every fourth 32-column group of the accumulator
 // Gate/up blocks interleave their rows: tensor-memory lane 2n holds gate row
@@ -52,10 +52,14 @@
 //
 // Synchronisation, per CTA unless stated:
 //   full[s]     this CTA's codes and routed rows of stage s landed
-//   empty[s]    the pair's MMAs have consumed stage s (one multicast commit)
-//   ready[a]    in the even CTA only: both CTAs' dequantising warps have
-//               filled A slot a (8 arrivals, 4 remote)
-//   aempty[a]   the pair's MMAs reading A slot a completed (multicast commit)
+//   empty[s]    the pair's MMAs have consumed stage s and its two A slots
+//               (one multicast commit); the producer and the dequantising
+//               warps wait on it before reusing them
+//   ready[s]    in the even CTA only: both CTAs' dequantising warps have
+//               filled stage s's A slots (16 arrivals, 8 remote)
+// The MMA thread waits once and commits once per stage (eight MMAs): a wait,
+// a fence and a commit around every four MMAs cost about as much issue time
+// as the MMAs of a 128-row tile take (measured on a probe).
 //   accf        the accumulator holds a finished item (one multicast commit)
 //   acce        in the even CTA only: both CTAs' epilogues have read the
 //               accumulator (32 arrivals, 16 remote)
@@ -74,7 +78,7 @@ constexpr int XT_BK = 64;                                // K per step (one A sl
 constexpr int XT_SUB = 2;                                // steps per stage
 constexpr int XT_NMAX = 256;                             // routed rows per tile
 constexpr int XT_STAGES = 4;                             // shared-memory ring
-constexpr int XT_ASLOTS = 8;                             // A slots in tensor memory
+constexpr int XT_ASLOTS = 2 * XT_STAGES;                 // A slots in tensor memory: two per stage
 constexpr int XT_B_SUB = XT_NMAX / 2 * 128;              // this CTA's half of the rows x 64 f16
 constexpr int XT_B_BYTES = XT_SUB * XT_B_SUB;
 constexpr int XT_C_BYTES = 128 * 64;                     // 128 weight rows x 64 code bytes (128 K)
@@ -89,15 +93,15 @@ constexpr int XT_EPI_WARP0 = XT_DQ_WARP0 + XT_DQ_WARPS;
 constexpr int XT_PROD1_WARP = XT_EPI_WARP0 + XT_EPI_WARPS;   // the second producer
 constexpr int XT_THREADS = (XT_PROD1_WARP + 1) * 32;
 constexpr int XT_EPI_THREADS = XT_EPI_WARPS * 32;
-// full[S], empty[S], ready[A], aempty[A], accumulator full / empty, MMA drain
-constexpr int XT_BARS = 2 * XT_STAGES + 2 * XT_ASLOTS + 3;
+// full[S], empty[S], ready[S], accumulator full / empty, MMA drain
+constexpr int XT_BARS = 3 * XT_STAGES + 3;
 // output staging: per epilogue warp two buffers of 32 routed rows x 32 bf16
 // (gate/up uses 16 of the 32 columns); per-row multipliers
 constexpr int XT_STG_BYTES = 32 * 64;
 constexpr int XT_EPI_BYTES = XT_EPI_WARPS * 2 * XT_STG_BYTES + XT_NMAX * 4;
 constexpr int XT_SMEM = XT_STAGES * XT_STAGE_BYTES + XT_EPI_BYTES + 1024 /*alignment*/ + 256 /*barriers, slot, flag*/;
 static_assert(XT_A_COL0 + XT_ASLOTS * 32 <= XT_TMEM_COLS, "tensor memory columns");
-static_assert(XT_SUB == 2 && XT_ASLOTS % 2 == 0, "the two dequant groups take the two steps of a stage");
+static_assert(XT_SUB == 2 && XT_ASLOTS == XT_SUB * XT_STAGES, "the two dequant groups take the two steps of a stage");
 // a second CTA never fits an SM's 228 KB of shared memory (nor its registers),
 // so the CTA's allocation of all 512 tensor-memory columns never waits
 static_assert(2 * (XT_SMEM + 1024) > 228 * 1024, "one CTA per SM");
@@ -163,9 +167,8 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + XT_BARS) + 1;
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (XT_STAGES + s); };
-  auto ready_bar = [&](int a) { return bar_base + 8u * (2 * XT_STAGES + a); };
-  auto aempty_bar = [&](int a) { return bar_base + 8u * (2 * XT_STAGES + XT_ASLOTS + a); };
-  const uint32_t accf_bar = bar_base + 8u * (2 * XT_STAGES + 2 * XT_ASLOTS);
+  auto ready_bar = [&](int s) { return bar_base + 8u * (2 * XT_STAGES + s); };
+  const uint32_t accf_bar = bar_base + 8u * (3 * XT_STAGES);
   const uint32_t acce_bar = accf_bar + 8u;
   const uint32_t drain_bar = accf_bar + 16u;
   auto stage_b = [&](int s) { return base + s * XT_STAGE_BYTES; };
@@ -181,10 +184,7 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
     for (int s = 0; s < XT_STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
-    }
-    for (int a = 0; a < XT_ASLOTS; ++a) {
-      mbar_init(ready_bar(a), 2 * XT_DQ_GROUP);
-      mbar_init(aempty_bar(a), 1);
+      mbar_init(ready_bar(s), 2 * XT_DQ_WARPS);
     }
     mbar_init(accf_bar, 1);
     mbar_init(acce_bar, 2 * XT_EPI_WARPS);
@@ -252,24 +252,24 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
         const int nbox = (p.tile_rows[t] + 31) / 32;
         // kind::f16: f16 A and B, fp32 D, both K-major; N >> 3 at bit 17, M >> 4 at bit 24
         const uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(nbox * 32 >> 3) << 17) | (uint32_t(256 >> 4) << 24);
-        for (int ks = 0; ks < n_st && ok; ++ks, ++it) {
+        for (int ks = 0; ks < n_st; ++ks, ++it) {
           const int s = it % XT_STAGES;
-          for (int q = 0; q < XT_SUB; ++q) {
-            const int j = XT_SUB * it + q, a = j % XT_ASLOTS;
-            // the dequantising warps of both CTAs arrive only after their stage's copies landed
-            if (!mbar_wait_cluster_bounded(ready_bar(a), (j / XT_ASLOTS) & 1, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+          // the dequantising warps of both CTAs arrive only after their stage's copies landed
+          if (!mbar_wait_cluster_bounded(ready_bar(s), (it / XT_STAGES) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = tmem + XT_A_COL0 + static_cast<uint32_t>(s) * (XT_SUB * 32);
+          const uint64_t b0 = smem_desc(stage_b(s), 16, 1024, 2);
+#pragma unroll
+          for (int q = 0; q < XT_SUB; ++q)
 #pragma unroll
             for (int k = 0; k < XT_BK / 16; ++k)
-              tc_mma_f16_tmem_a_pair(tmem, tmem + XT_A_COL0 + a * 32 + 8 * k,
-                                     smem_desc(stage_b(s) + q * XT_B_SUB + 32 * k, 16, 1024, 2), idesc,
-                                     (ks > 0 || q > 0 || k > 0) ? 1u : 0u);
-            tc_commit_pair(aempty_bar(a));
-          }
-          if (ok) tc_commit_pair(empty_bar(s));
+              // A: 8 columns per 16 K; B: the descriptor's address field counts 16 bytes
+              tc_mma_f16_tmem_a_pair(tmem, a0 + 32 * q + 8 * k, b0 + static_cast<uint64_t>((q * XT_B_SUB + 32 * k) >> 4),
+                                     idesc, (ks > 0 || q > 0 || k > 0) ? 1u : 0u);
+          tc_commit_pair(empty_bar(s));
         }
         if (ok) tc_commit_pair(accf_bar);
       }
@@ -303,14 +303,14 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
           if (ks / 2 + 1 < n_st / 2) sc_next = __ldg(sgrp + ks / 2 + 1);
         }
         const int it = it0 + ks, s = it % XT_STAGES;
-        const int j = XT_SUB * it + grp, a = j % XT_ASLOTS;
+        const int a = XT_SUB * s + grp;               // this step's A slot
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(full_bar(s), (it / XT_STAGES) & 1, abort_flag, p.status))) {
           ok = false;
           break;
         }
-        // the A slot is free once the MMAs of step j - XT_ASLOTS completed
-        if (j >= XT_ASLOTS &&
-            !__all_sync(0xffffffffu, mbar_wait_cluster_bounded(aempty_bar(a), ((j / XT_ASLOTS) - 1) & 1, abort_flag,
+        // the A slot is free once the MMAs of stage it - XT_STAGES completed
+        if (it >= XT_STAGES &&
+            !__all_sync(0xffffffffu, mbar_wait_cluster_bounded(empty_bar(s), ((it / XT_STAGES) - 1) & 1, abort_flag,
                                                                p.status))) {
           ok = false;
           break;
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(ready_bar(a), 0);
+        if (lane == 0) mbar_arrive_cluster(ready_bar(s), 0);
       }
     }
   } else if (warp >= XT_EPI_WARP0 && warp < XT_EPI_WARP0 + XT_EPI_WARPS) {
