@@ -307,11 +307,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const int atoms = min(4, k_atoms_total - 4 * ks);
           const uint32_t sf_col = tmem + SF_TMEM_BASE + s * SF_COLS_PER_STAGE;
-          for (int k = 0; k < atoms; ++k) {
-            const uint64_t adesc = smem_desc(stage_a(s) + 32 * k, 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(stage_b(s) + 32 * k, 16, 1024, 2);
-            tc_mma_mxf4nvf4(tmem, adesc, bdesc, IDESC, sf_col + 4 * k, sf_col + 16 + 8 * k,
-                            (ks > 0 || k > 0) ? 1u : 0u);
+          // descriptors by offset (the address field counts 16 bytes); a full
+          // stage as straight-line code: the MMA thread's issue time per MMA
+          // in a runtime-count loop exceeded what an N = 256 MMA takes
+          const uint64_t adesc = smem_desc(stage_a(s), 16, 1024, 2), bdesc = smem_desc(stage_b(s), 16, 1024, 2);
+          if (atoms == 4) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc_mma_mxf4nvf4(tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, sf_col + 4 * k, sf_col + 16 + 8 * k,
+                              (ks > 0 || k > 0) ? 1u : 0u);
+          } else {
+            for (int k = 0; k < atoms; ++k)
+              tc_mma_mxf4nvf4(tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, sf_col + 4 * k, sf_col + 16 + 8 * k,
+                              (ks > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit(empty_bar(s));
         }
@@ -612,10 +620,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const int atoms = min(4, k_atoms_total - 4 * ks);
           const uint32_t sf_col = tmem + SF_TMEM_BASE + s * SF_COLS_PER_STAGE;
-          for (int k = 0; k < atoms; ++k) {
-            const uint64_t adesc = smem_desc(stage_a(s) + 32 * k, 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(stage_b(s) + 32 * k, 16, 1024, 2);
-            tc_mma_pair(tmem, adesc, bdesc, sf_col + 4 * k, sf_col + 16 + 8 * k, (ks > 0 || k > 0) ? 1u : 0u);
+          // descriptors by offset (the address field counts 16 bytes); a full
+          // stage as straight-line code (see gemm_w4a4_kernel). This costs the
+          // bf16-output instantiation a 40-byte spill (register cap 128 at
+          // 512 threads), measured cheaper than the runtime-count loop.
+          const uint64_t adesc = smem_desc(stage_a(s), 16, 1024, 2), bdesc = smem_desc(stage_b(s), 16, 1024, 2);
+          if (atoms == 4) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc_mma_pair(tmem, adesc + 2 * k, bdesc + 2 * k, sf_col + 4 * k, sf_col + 16 + 8 * k,
+                          (ks > 0 || k > 0) ? 1u : 0u);
+          } else {
+            for (int k = 0; k < atoms; ++k)
+              tc_mma_pair(tmem, adesc + 2 * k, bdesc + 2 * k, sf_col + 4 * k, sf_col + 16 + 8 * k,
+                          (ks > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit_pair(empty_bar(s));
         }
@@ -912,11 +930,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const int atoms = min(4, k_atoms_total - 4 * ks);
           const uint32_t sf_col = tmem + SF_TMEM_BASE + s * SF_COLS_PER_STAGE;
-          for (int k = 0; k < atoms; ++k) {
-            const uint64_t adesc = smem_desc(stage_a(s) + 32 * k, 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(stage_b(s) + 32 * k, 16, 1024, 2);
-            tc_mma_mxf4nvf4(tmem, adesc, bdesc, IDESC, sf_col + 4 * k, sf_col + 16 + 8 * k,
-                            (ks > 0 || k > 0) ? 1u : 0u);
+          // descriptors by offset (the address field counts 16 bytes); a full
+          // stage as straight-line code: the MMA thread's issue time per MMA
+          // in a runtime-count loop exceeded what an N = 256 MMA takes
+          const uint64_t adesc = smem_desc(stage_a(s), 16, 1024, 2), bdesc = smem_desc(stage_b(s), 16, 1024, 2);
+          if (atoms == 4) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc_mma_mxf4nvf4(tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, sf_col + 4 * k, sf_col + 16 + 8 * k,
+                              (ks > 0 || k > 0) ? 1u : 0u);
+          } else {
+            for (int k = 0; k < atoms; ++k)
+              tc_mma_mxf4nvf4(tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, sf_col + 4 * k, sf_col + 16 + 8 * k,
+                              (ks > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit(empty_bar(s));
         }
