@@ -64,6 +64,59 @@ __global__ void route_kernel(const float* logits, int64_t T, int E, int topk, in
   }
 }
 
+// The same routing with the token's probabilities held in registers (E <=
+// 32 EPL): the logits are read and each probability computed once, by the
+// same expressions as route_kernel, so the ids and weights are identical.
+template <int EPL>
+__global__ void route_reg_kernel(const float* logits, int64_t T, int E, int topk, int32_t* ids, float* weights) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* l = logits + t * E;
+  float v[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? l[e] : -INFINITY;
+  }
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) mx = fmaxf(mx, v[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i)
+    if (lane + 32 * i < E) sum += expf(v[i] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  unsigned long long key[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    const float pr = expf(v[i] - mx) / sum;
+    key[i] = e < E ? (static_cast<unsigned long long>(float_order_key(pr)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e))
+                   : 0ull;
+  }
+  unsigned long long prev = ~0ull;
+  for (int j = 0; j < topk; ++j) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (key[i] < prev && key[i] > best) best = key[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
+    }
+    prev = best;
+    if (lane == 0) {
+      ids[t * topk + j] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(best));
+      weights[t * topk + j] = float_from_order_key(static_cast<uint32_t>(best >> 32));
+    }
+  }
+}
+
 // tile sizes of the routing plan: the W4A4 expert GEMM takes tiles of up to
 // 128 routed rows (its MMAs are M = 128 over routed rows), the W4A16
 // tensor-core kernel tiles of up to XT_NMAX; the tile table is sized for the
@@ -658,9 +711,14 @@ int combine(const MoeWs& m, const float* w, int64_t T, int topk, int64_t H, uint
 int launch_moe_route(const float* logits, int64_t T, int E, int topk, int32_t* ids, float* weights,
                      cudaStream_t stream) {
   if (T == 0) return NVFP4_OK;
-  const int warps = 8;
-  route_kernel<<<static_cast<unsigned>(ceil_div(T, warps)), warps * 32, 0, stream>>>(logits, T, E, topk, ids,
-                                                                                   weights);
+  const int warps = 4;
+  const unsigned grid = static_cast<unsigned>(ceil_div(T, warps));
+  if (E <= 128)
+    route_reg_kernel<4><<<grid, warps * 32, 0, stream>>>(logits, T, E, topk, ids, weights);
+  else if (E <= 256)
+    route_reg_kernel<8><<<grid, warps * 32, 0, stream>>>(logits, T, E, topk, ids, weights);
+  else
+    route_kernel<<<grid, warps * 32, 0, stream>>>(logits, T, E, topk, ids, weights);
   return from_cuda(cudaGetLastError());
 }
 

@@ -12,18 +12,22 @@ pytestmark = pytest.mark.gpu
 TOL = 1e-2
 
 
-def test_route_matches_oracle():
+# (T, E, k): expert counts held in registers (E <= 128, E <= 256, with lanes
+# past E) and the generic kernel (E > 256); token counts off the CTA size
+@pytest.mark.parametrize("T,E,k", [(512, 128, 8), (37, 200, 4), (64, 300, 6), (33, 32, 2), (5, 256, 8)])
+def test_route_matches_oracle(T, E, k):
     m = nv()
-    logits = synth.normal_f32((512, 128), 1.0, seed=8)
-    ids, w = m.moe_route(logits.to(DEV), 8)
-    oids, ow = O.moe_route(logits.numpy(), 8)
+    logits = synth.normal_f32((T, E), 1.0, seed=8 + E)
+    ids, w = m.moe_route(logits.to(DEV), k)
+    oids, ow = O.moe_route(logits.numpy(), k)
     ids, w = ids.cpu().numpy(), w.cpu().numpy()
     p = torch.softmax(logits.double(), 1).numpy()
-    for t in range(512):
+    for t in range(T):
         ps = np.sort(p[t])[::-1]
-        gaps = np.abs(np.diff(ps[:9]))
-        if gaps.min() > 1e-6:            # no near-tie among the top 9
+        gaps = np.abs(np.diff(ps[:k + 1]))
+        if gaps.min() > 1e-6:            # no near-tie among the top k + 1
             assert list(ids[t]) == list(oids[t])
+        assert len(set(ids[t].tolist())) == k and all(0 <= i < E for i in ids[t])
         np.testing.assert_allclose(w[t], p[t, ids[t]], rtol=1e-5)
 
 
