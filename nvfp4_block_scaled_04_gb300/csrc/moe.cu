@@ -122,6 +122,12 @@ __global__ void route_reg_kernel(const float* logits, int64_t T, int E, int topk
 // tensor-core kernel tiles of up to XT_NMAX; the tile table is sized for the
 // smaller
 constexpr int PLAN_TILE_MIN = 128;
+// the cooperative routing plan: at most this many CTAs, each with a slice of
+// at least PLAN_COOP_SLICE routed slots
+constexpr int PLAN_COOP_MAX_G = 128;
+constexpr int PLAN_COOP_SLICE = 512;
+constexpr int PLAN_COOP_THREADS = 512;
+constexpr int PLAN_COOP_MAX_E = 256;
 
 struct MoeWs {
   int* chunk_count;   // [1]
@@ -134,6 +140,8 @@ struct MoeWs {
   int* tile_rows;     // [max_tiles]
   int* row_of;        // [padded rows] token id or -1
   int* pos_of;        // [T*k]
+  int* plan_hist;     // [PLAN_COOP_MAX_G][E]: the cooperative plan's per-CTA expert counts
+  unsigned int* plan_bar;   // [1]: its grid barrier
   int* pexp1;         // [padded rows]
   int* pexp2;         // [padded rows]
   uint4* xfrag1;      // tokens, K = H
@@ -181,6 +189,8 @@ MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
   w.tile_rows = reinterpret_cast<int*>(take(w.max_tiles * sizeof(int)));
   w.row_of = reinterpret_cast<int*>(take(rows * sizeof(int)));
   w.pos_of = reinterpret_cast<int*>(take(R * sizeof(int)));
+  w.plan_hist = reinterpret_cast<int*>(take(static_cast<size_t>(PLAN_COOP_MAX_G) * E * sizeof(int)));
+  w.plan_bar = reinterpret_cast<unsigned int*>(take(sizeof(unsigned int)));
   if (!w4a4) {
     w.pexp1 = reinterpret_cast<int*>(take(rows * sizeof(int)));
     w.pexp2 = reinterpret_cast<int*>(take(rows * sizeof(int)));
@@ -447,6 +457,150 @@ __global__ void __launch_bounds__(PLAN_THREADS) route_plan_kernel(const int32_t*
   }
 }
 
+// The routing plan over G CTAs of one cooperative launch (all resident), for
+// many routed slots and E <= PLAN_COOP_MAX_E (the single-CTA plan spent ~20 us
+// on 32,768 slots). CTA g counts the experts of its slice of the slots into
+// hist[g][*]; after one grid barrier every CTA reads the whole count table,
+// takes each expert's padded offset (block scan) and its own offset within
+// each expert (the counts of the CTAs before it), and places its slots; CTA 0
+// also writes the chunk and tile tables and marks each expert's padding rows
+// with -1. The results are the single-CTA plan's up to the order of rows
+// within an expert, which no output depends on. The barrier wait is bounded:
+// a CTA that gives up records NVFP4_ERR_TIMEOUT and leaves.
+__global__ void __launch_bounds__(PLAN_COOP_THREADS) route_plan_coop_kernel(
+    const int32_t* ids, int64_t R, int topk, int E, int* poff, int* chunk_count, int* chunk_expert, int* chunk_rows,
+    int* tile_count, int* tile_expert, int* tile_row0, int* tile_rows, int* row_of, int* pos_of, int* hist,
+    unsigned int* bar, int* status, int tile_max) {
+  __shared__ int s_cnt[PLAN_COOP_MAX_E];   // this CTA's counts, then its cursors
+  __shared__ int s_off[PLAN_COOP_MAX_E];   // expert base + this CTA's offset within the expert
+  __shared__ int s_tot[PLAN_COOP_MAX_E];
+  __shared__ int s_pb[PLAN_COOP_THREADS], s_pt[PLAN_COOP_THREADS];   // partial sums [part][E]
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, G = static_cast<int>(gridDim.x), g = static_cast<int>(blockIdx.x);
+  const int64_t slice = (R + G - 1) / G;
+  const int64_t i_begin = g * slice, i_end = i_begin + slice < R ? i_begin + slice : R;
+  for (int e = tid; e < E; e += PLAN_COOP_THREADS) s_cnt[e] = 0;
+  if (tid == 0) s_abort = 0;
+  __syncthreads();
+  for (int64_t i = i_begin + tid; i < i_end; i += PLAN_COOP_THREADS) {
+    const int e = ids[i];
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += PLAN_COOP_THREADS) hist[g * E + e] = s_cnt[e];
+  // grid barrier: every CTA's counts are in hist
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    atomicAdd(bar, 1u);
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 0; *reinterpret_cast<volatile unsigned int*>(bar) < static_cast<unsigned int>(G); ++n) {
+      if ((n & 63) == 63 && globaltimer() - t0 > WAIT_LIMIT_NS) {
+        atomicExch(status, NVFP4_ERR_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      __nanosleep(32);
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  if (s_abort) return;
+  // totals and this CTA's offset within each expert: `parts` threads per
+  // expert, each summing every parts-th CTA's count (independent loads)
+  const int parts = PLAN_COOP_THREADS / E;   // >= 2
+  if (tid < parts * E) {
+    const int e = tid % E, part = tid / E;
+    int before = 0, tot = 0;
+#pragma unroll 4
+    for (int h = part; h < G; h += parts) {
+      const int c = __ldcg(hist + h * E + e);
+      before += h < g ? c : 0;
+      tot += c;
+    }
+    s_pb[part * E + e] = before;
+    s_pt[part * E + e] = tot;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += PLAN_COOP_THREADS) {
+    int before = 0, tot = 0;
+    for (int part = 0; part < parts; ++part) before += s_pb[part * E + e], tot += s_pt[part * E + e];
+    s_tot[e] = tot;
+    s_off[e] = before;
+    s_cnt[e] = 0;
+  }
+  __syncthreads();
+  // expert base offsets (padded to GV_MCHUNK rows): a scan by warp 0, E <= 256
+  if (tid < 32) {
+    int base = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + tid;
+      const int pr = e < E ? (s_tot[e] + GV_MCHUNK - 1) / GV_MCHUNK * GV_MCHUNK : 0;
+      int inc = pr;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, inc, o);
+        if (tid >= o) inc += a;
+      }
+      if (e < E) {
+        const int ex = base + inc - pr;   // exclusive
+        s_off[e] += ex;
+        if (g == 0) poff[e] = ex;
+      }
+      base += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (g == 0 && tid == 0) *chunk_count = base / GV_MCHUNK;
+  }
+  __syncthreads();
+  if (g == 0) {
+    // tables (one thread per expert; tile index from a scan of tile counts)
+    if (tid < 32) {
+      int tbase = 0;
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + tid;
+        const int n = e < E ? s_tot[e] : 0;
+        const int nt = (n + tile_max - 1) / tile_max;
+        int inc = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int a = __shfl_up_sync(0xffffffffu, inc, o);
+          if (tid >= o) inc += a;
+        }
+        if (e < E) {
+          const int acc = s_off[e];   // CTA 0: its own offset within each expert is 0
+          int tiles = tbase + inc - nt;
+          const int sz = nt > 0 ? ((n + nt - 1) / nt + 31) / 32 * 32 : tile_max;
+          for (int r = 0; r < n; r += sz, ++tiles) {
+            tile_expert[tiles] = e;
+            tile_row0[tiles] = acc + r;
+            tile_rows[tiles] = min(sz, n - r);
+          }
+          for (int c = 0; c * GV_MCHUNK < n; ++c) {
+            chunk_expert[acc / GV_MCHUNK + c] = e;
+            chunk_rows[acc / GV_MCHUNK + c] = min(GV_MCHUNK, n - c * GV_MCHUNK);
+          }
+          // the expert's padding rows hold no token
+          for (int r = n; r < (n + GV_MCHUNK - 1) / GV_MCHUNK * GV_MCHUNK; ++r) row_of[acc + r] = -1;
+        }
+        tbase += __shfl_sync(0xffffffffu, inc, 31);
+      }
+      if (tid == 0) *tile_count = tbase;
+    }
+  }
+  // place this CTA's slots
+  for (int64_t i = i_begin + tid; i < i_end; i += PLAN_COOP_THREADS) {
+    const int e = ids[i];
+    if (e < 0 || e >= E) {
+      pos_of[i] = -1;
+      atomicExch(status, NVFP4_ERR_INVALID_ARG);
+      continue;
+    }
+    const int pos = s_off[e] + atomicAdd(&s_cnt[e], 1);
+    row_of[pos] = static_cast<int>(static_cast<uint32_t>(i) / static_cast<uint32_t>(topk));
+    pos_of[i] = pos;
+  }
+}
+
 template <bool PRIVATE, bool SMEM_ROWS>
 int launch_route_plan_t(const int32_t* ids, int64_t R, int topk, int64_t E, const MoeWs& m, int tile_max,
                         cudaStream_t stream) {
@@ -465,6 +619,26 @@ int launch_route_plan_t(const int32_t* ids, int64_t R, int topk, int64_t E, cons
 // tile_max: a multiple of 32, at least PLAN_TILE_MIN
 int launch_route_plan(const int32_t* ids, int64_t R, int topk, int64_t E, const MoeWs& m, int tile_max,
                       cudaStream_t stream) {
+  if (E <= PLAN_COOP_MAX_E && R >= 16LL * PLAN_COOP_SLICE) {
+    int64_t G = (R + PLAN_COOP_SLICE - 1) / PLAN_COOP_SLICE;
+    const int64_t cap = sm_count() < PLAN_COOP_MAX_G ? sm_count() : PLAN_COOP_MAX_G;   // one CTA per SM fits
+    if (G > cap) G = cap;
+    if (cudaMemsetAsync(m.plan_bar, 0, sizeof(unsigned int), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(G));
+    cfg.blockDim = dim3(PLAN_COOP_THREADS);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int* status = device_status_ptr();
+    const int Ei = static_cast<int>(E);
+    return from_cuda(cudaLaunchKernelEx(&cfg, route_plan_coop_kernel, ids, R, topk, Ei, m.poff, m.chunk_count,
+                                        m.chunk_expert, m.chunk_rows, m.tile_count, m.tile_expert, m.tile_row0,
+                                        m.tile_rows, m.row_of, m.pos_of, m.plan_hist, m.plan_bar, status, tile_max));
+  }
   const bool priv = E <= PLAN_PRIVATE_MAX_E;
   const bool staged = R + GV_MCHUNK * E <= PLAN_SMEM_ROWS_MAX;
   if (priv && staged) return launch_route_plan_t<true, true>(ids, R, topk, E, m, tile_max, stream);

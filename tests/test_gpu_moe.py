@@ -173,12 +173,13 @@ def test_moe_config_t4096_sampled_tokens():
     assert O.rel_fro(out[toks], ref) <= TOL
 
 
-@pytest.mark.parametrize("T,E,H,I", [(40, 8, 128, 128), (512, 4, 256, 256)])
+@pytest.mark.parametrize("T,E,H,I", [(40, 8, 128, 128), (512, 4, 256, 256), (4096, 4, 256, 256)])
 def test_out_of_range_expert_ids_are_dropped_and_reported(T, E, H, I):
     """Slots whose expert id is -2, -1 or E contribute nothing, and the call
     reports NVFP4_ERR_INVALID_ARG in the device status word; the result equals
     the layer with those slots' weights set to zero. (512, 4, 256, 256) runs the
-    tensor-core path."""
+    tensor-core path; (4096, 4, 256, 256), 8192 routed slots, also the
+    routing plan over several CTAs."""
     m = nv()
     k = 2
     logits, x, w13, w2 = moe_case(T, E, H, I, k, seed=T + 7)
