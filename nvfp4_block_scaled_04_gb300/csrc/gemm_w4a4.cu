@@ -976,6 +976,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_ld_32cols(tmem + lanes + static_cast<uint32_t>(64 * half + 32 * c), g);
           tc_ld_32cols(tmem + lanes + static_cast<uint32_t>(128 + 64 * half + 32 * c), u);
           tc_wait_ld();
+          if (c == 1) {
+            // the accumulator's last reads: the next item's MMAs may start
+            // while this warp does the SiLU math and the stores
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar);
+          }
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             const float g0 = __uint_as_float(g[2 * q]) * scale, g1 = __uint_as_float(g[2 * q + 1]) * scale;
@@ -990,9 +997,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             hmax = max(hmax, max(b & 0x7FFFu, (b >> 16) & 0x7FFFu));
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(acce_bar);
         const bool valid = i < nrows;
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(p.h_out + row * p.inter + j * 128 + 64 * half);
@@ -1002,30 +1006,28 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t m = __reduce_max_sync(0xffffffffu, valid ? hmax : 0u);
         if (lane == 0 && m != 0u) atomicMax(p.amax_bits, m << 16);
       } else {
-        // each 32-column chunk is stored as soon as it is read; the
-        // accumulator is released after the last read
+        // the row's 128 columns are read and packed to bf16 before any store,
+        // and the accumulator released then: with the stores between the
+        // reads the next item's MMAs waited for them (70% of the MMA thread's
+        // time in the down GEMM)
         uint4* dst = reinterpret_cast<uint4*>(p.y_out + row * p.hidden + j * 256 + half * 128);
+        uint32_t packed[64];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
           tc_ld_32cols(tmem + lanes + static_cast<uint32_t>(half * 128 + 32 * c), r);
           tc_wait_ld();
-          if (c == 3) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar);
-          }
-          if (i < nrows) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t b[4];
+          for (int q = 0; q < 16; ++q)
+            packed[16 * c + q] = f32x2_to_bf16x2(__uint_as_float(r[2 * q]) * scale, __uint_as_float(r[2 * q + 1]) * scale);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar);
+        if (i < nrows) {
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                b[e] = f32x2_to_bf16x2(__uint_as_float(r[8 * q + 2 * e]) * scale,
-                                       __uint_as_float(r[8 * q + 2 * e + 1]) * scale);
-              dst[4 * c + q] = make_uint4(b[0], b[1], b[2], b[3]);
-            }
-          }
+          for (int q = 0; q < 16; ++q)
+            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
         }
       }
     }
