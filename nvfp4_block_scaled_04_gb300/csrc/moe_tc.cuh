@@ -106,6 +106,7 @@ static_assert(XT_SUB == 2 && XT_ASLOTS == XT_SUB * XT_STAGES, "the two dequant g
 // so the CTA's allocation of all 512 tensor-memory columns never waits
 static_assert(2 * (XT_SMEM + 1024) > 228 * 1024, "one CTA per SM");
 static_assert(XT_BARS * 8 + 16 <= 256, "barrier area");
+static_assert(XT_NMAX / 32 <= 2 * 4, "at most two 32-column groups per epilogue warp (four warps per lane quarter)");
 
 struct MoeTcParams {
   const uint8_t* scales;   // row-major block scales of the stacked weights [E * rows_per_expert][K / 16]
@@ -365,23 +366,21 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
       const bool got = __all_sync(0xffffffffu, mbar_wait_cluster_bounded(accf_bar, item & 1, abort_flag, p.status));
       if (!xt_all_epilogue(got && *abort_flag == 0)) break;
       tc_fence_after();
-      for (int j = ch; j < nbox; j += 4, ++nstore) {
-        uint32_t a[32];
-        tc_ld_32cols(tmem + lanes + static_cast<uint32_t>(32 * j), a);
-        tc_wait_ld();
-        if (j + 4 >= nbox) {
-          // the accumulator's last reads of this item: let the MMAs of the next one start
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acce_bar, 0);
-        }
-        // this warp's staging buffer: the tensor store that last read it is done
-        const uint32_t buf = stg + static_cast<uint32_t>(nstore & 1) * XT_STG_BYTES;
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        __syncwarp();
-        // staging layout: routed row c of the group at buf + c * 2 OCOLS, bf16 columns
+      // phase A: read this warp's column groups (at most two: j = ch, ch + 4)
+      // and form their outputs as bf16 pairs in registers, then release the
+      // accumulator; phase B stages and stores them. (Staging and storing a
+      // group before reading the next held the next item's MMAs: the MMA
+      // thread waited for the epilogue 16% / 30% of its time.)
+      constexpr int OW = GATEUP ? 8 : 16;   // output words of a group per thread
+      uint32_t ob[2][OW];
+#pragma unroll
+      for (int g2 = 0; g2 < 2; ++g2) {
+        const int j = ch + 4 * g2;
+        if (j >= nbox) continue;
         if (GATEUP) {
-          const int n = lane >> 1;
+          uint32_t a[32];
+          tc_ld_32cols(tmem + lanes + static_cast<uint32_t>(32 * j), a);
+          tc_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             // even lane (gate): routed row 2i; odd lane (up): routed row 2i + 1
@@ -392,13 +391,49 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
             const float m = mulv[32 * j + c];
             const float g = __uint_as_float((lane & 1) ? other : mine) * m;
             const float u = __uint_as_float((lane & 1) ? mine : other) * m;
-            const uint16_t h = static_cast<uint16_t>(f32_to_bf16_bits(__fdividef(g, 1.0f + __expf(-g)) * u));
+            const uint32_t h = f32_to_bf16_bits(__fdividef(g, 1.0f + __expf(-g)) * u);
+            ob[g2][i >> 1] = (i & 1) ? (ob[g2][i >> 1] | (h << 16)) : h;
+          }
+        } else {
+          // in 16-column halves (registers)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t a[16];
+            tc_ld_16cols(tmem + lanes + static_cast<uint32_t>(32 * j + 16 * hh), a);
+            tc_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 16; c += 2)
+              ob[g2][8 * hh + (c >> 1)] = f32x2_to_bf16x2(__uint_as_float(a[c]) * mulv[32 * j + 16 * hh + c],
+                                                          __uint_as_float(a[c + 1]) * mulv[32 * j + 16 * hh + c + 1]);
+          }
+        }
+      }
+      // the accumulator's last reads of this item: let the MMAs of the next one start
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acce_bar, 0);
+#pragma unroll
+      for (int g2 = 0; g2 < 2; ++g2) {
+        const int j = ch + 4 * g2;
+        if (j >= nbox) continue;
+        // this warp's staging buffer: the tensor store that last read it is done
+        const uint32_t buf = stg + static_cast<uint32_t>(nstore & 1) * XT_STG_BYTES;
+        ++nstore;
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+        // staging layout: routed row c of the group at buf + c * 2 OCOLS, bf16 columns
+        if (GATEUP) {
+          const int n = lane >> 1;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = 2 * i + (lane & 1);
+            const uint16_t h = static_cast<uint16_t>(ob[g2][i >> 1] >> (16 * (i & 1)));
             asm volatile("st.shared.b16 [%0], %1;" ::"r"(buf + c * (2 * OCOLS) + 2 * n), "h"(h) : "memory");
           }
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const uint16_t y = static_cast<uint16_t>(f32_to_bf16_bits(__uint_as_float(a[c]) * mulv[32 * j + c]));
+            const uint16_t y = static_cast<uint16_t>(ob[g2][c >> 1] >> (16 * (c & 1)));
             asm volatile("st.shared.b16 [%0], %1;" ::"r"(buf + c * (2 * OCOLS) + 2 * lane), "h"(y) : "memory");
           }
         }
@@ -422,12 +457,6 @@ __global__ void __launch_bounds__(XT_THREADS, 1)
               reinterpret_cast<uint4*>(dst)[q] = lds128(buf + c * (2 * OCOLS) + 16 * q);
           }
         }
-      }
-      if (nbox <= ch) {
-        // no column group for this warp in this item: it still releases the accumulator
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(acce_bar, 0);
       }
     }
     // stores complete before the CTA exits
