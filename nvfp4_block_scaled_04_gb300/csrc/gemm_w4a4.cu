@@ -1247,6 +1247,315 @@ int launch_w4a4_epi(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t* 
   return from_cuda(cudaGetLastError());
 }
 
+// The grouped expert GEMM on CTA pairs (cta_group::2), as gemm_w4a4_pair_kernel
+// does for one matrix: a work item is (tile t of up to 256 routed rows of one
+// expert, weight block j of 256 rows); the even CTA takes routed rows
+// [0, 128) of the tile and the odd one [128, 256), each loads one 128-row half
+// of the weight block (gate/up: the gate rows in the even CTA, the matching
+// up rows in the odd one; down: rows [256 j, +128) and [256 j + 128, +128)),
+// both hold the whole block's scales, and the even CTA's thread issues the
+// M = 256 MMAs. Per stage an SM now takes in 38 KB where the one-CTA kernel
+// took 54 KB for the same MMA work (the copies bound it). The routed rows are
+// tile-major with 256-row tiles (128-row MMA-layout scale strips 2t, 2t + 1).
+// Epilogue per warp (32 routed rows, one lane quarter): read and pack the
+// accumulator, release it, then store through a 4 KB staging box and a TMA
+// store (128B swizzle), or with plain stores where the box would reach past
+// the tile's rows (the next tile's rows follow in the plan's order).
+template <bool GATEUP>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_w4a4_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                             const __grid_constant__ CUtensorMap map_out, const GroupedW4A4Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t out_base = base + P_STAGES * P_STAGE_BYTES;   // 1024-aligned staging boxes
+  const uint32_t bar_base = out_base + EPI_WARPS * P_OUT_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + P_STAGES * P_STAGE_BYTES + EPI_WARPS * P_OUT_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * P_STAGES + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * P_STAGES + 3);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (P_STAGES + s); };
+  auto ready_bar = [&](int s) { return bar_base + 8u * (2 * P_STAGES + s); };
+  const uint32_t accf_bar = bar_base + 8u * (3 * P_STAGES);
+  const uint32_t acce_bar = bar_base + 8u * (3 * P_STAGES + 1);
+  auto stage_a = [&](int s) { return base + s * P_STAGE_BYTES; };
+  auto stage_b = [&](int s) { return base + s * P_STAGE_BYTES + A_BYTES; };
+  auto stage_sfa = [&](int s) { return base + s * P_STAGE_BYTES + A_BYTES + P_B_BYTES; };
+  auto stage_sfb = [&](int s) { return base + s * P_STAGE_BYTES + A_BYTES + P_B_BYTES + SFA_BYTES; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair_id = static_cast<int>(blockIdx.x >> 1), n_pairs = static_cast<int>(gridDim.x >> 1);
+  const int n_work = *p.tile_count * p.n_tiles;
+  const int n_k = (p.K + BK - 1) / BK;
+  const int k_atoms_total = p.K / 64;
+  const int64_t sf_row_stride = static_cast<int64_t>(k_atoms_total) * 512;   // bytes per 128-row scale strip
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(ready_bar(s), 2 * SF_WARPS);
+    }
+    mbar_init(accf_bar, 1);
+    mbar_init(acce_bar, 2 * EPI_WARPS);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_a) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_b) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&map_out) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();   // both CTAs' barriers and tensor memory exist before anything refers to them
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  int next_it = 0;
+  int mma_tiles = 0;
+  const int prod = warp == 0 ? 0 : (warp == 2 ? 1 : -1);
+
+  if (prod >= 0) {
+    if (lane == 0) {
+      int it = 0;
+      for (int w = pair_id; w < n_work && !*abort_flag; w += n_pairs) {
+        const int t = w / p.n_tiles, j = w - t * p.n_tiles;
+        const int e = p.tile_expert[t];
+        const int strip = 2 * t + static_cast<int>(rank);   // this CTA's 128 routed rows
+        // the weight block's two 128-row halves and their scale strips within expert e
+        const int rb0 = GATEUP ? j : 2 * j;
+        const int rb1 = GATEUP ? p.inter / 128 + j : 2 * j + 1;
+        const int ybase = e * p.rows_per_expert;
+        const int my_rb = rank == 0 ? rb0 : rb1;
+        const uint8_t* sfb_e = p.sfb + static_cast<int64_t>(e) * p.sfb_expert_bytes;
+        bool ok = true;
+        for (int ks = 0; ks < n_k; ++ks, ++it) {
+          if ((it & 1) != prod) continue;
+          const int s = it % P_STAGES;
+          if (it >= P_STAGES && !mbar_wait_cluster(empty_bar(s), ((it / P_STAGES) - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int atoms = min(4, k_atoms_total - 4 * ks);
+          const uint32_t sf_bytes = static_cast<uint32_t>(atoms) * 512u;
+          mbar_arrive_expect_tx(full_bar(s), A_BYTES + P_B_BYTES + 3u * sf_bytes);
+          tma_load_2d(stage_a(s), &map_a, ks * 128, strip * BM, full_bar(s));
+          tma_load_2d(stage_b(s), &map_b, ks * 128, ybase + my_rb * 128, full_bar(s));
+          bulk_load(stage_sfa(s), p.sfa + strip * sf_row_stride + static_cast<int64_t>(ks) * 2048, sf_bytes,
+                    full_bar(s));
+          bulk_load(stage_sfb(s), sfb_e + rb0 * sf_row_stride + static_cast<int64_t>(ks) * 2048, sf_bytes,
+                    full_bar(s));
+          bulk_load(stage_sfb(s) + 2048, sfb_e + rb1 * sf_row_stride + static_cast<int64_t>(ks) * 2048, sf_bytes,
+                    full_bar(s));
+          next_it = it + 1;
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (rank == 0 && lane == 0) {
+      int it = 0;
+      for (int w = pair_id; w < n_work && !*abort_flag; w += n_pairs) {
+        // both CTAs' epilogues must have read the previous item's accumulator
+        if (mma_tiles > 0 && !mbar_wait_cluster(acce_bar, (mma_tiles - 1) & 1, abort_flag)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int ks = 0; ks < n_k; ++ks, ++it) {
+          const int s = it % P_STAGES;
+          // both CTAs' scale warps arrive only after their stage's copies landed
+          if (!mbar_wait_cluster(ready_bar(s), (it / P_STAGES) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int atoms = min(4, k_atoms_total - 4 * ks);
+          const uint32_t sf_col = tmem + SF_TMEM_BASE + s * SF_COLS_PER_STAGE;
+          const uint64_t adesc = smem_desc(stage_a(s), 16, 1024, 2), bdesc = smem_desc(stage_b(s), 16, 1024, 2);
+          if (atoms == 4) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc_mma_pair(tmem, adesc + 2 * k, bdesc + 2 * k, sf_col + 4 * k, sf_col + 16 + 8 * k,
+                          (ks > 0 || k > 0) ? 1u : 0u);
+          } else {
+            for (int k = 0; k < atoms; ++k)
+              tc_mma_pair(tmem, adesc + 2 * k, bdesc + 2 * k, sf_col + 4 * k, sf_col + 16 + 8 * k,
+                          (ks > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit_pair(empty_bar(s));
+        }
+        if (!ok) break;
+        tc_commit_pair(accf_bar);
+        ++mma_tiles;
+      }
+    }
+  } else if (warp < SF_WARP0) {
+    const int quarter = warp & 3;
+    const int half = (warp - EPI_WARP0) >> 2;
+    const uint32_t lanes = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t stage_out = out_base + static_cast<uint32_t>(warp - EPI_WARP0) * P_OUT_BYTES;
+    int done = 0;
+    for (int w = pair_id; w < n_work; w += n_pairs, ++done) {
+      const int t = w / p.n_tiles, j = w - t * p.n_tiles;
+      const int e = p.tile_expert[t];
+      const int nrows = p.tile_rows[t];
+      const int li0 = 128 * static_cast<int>(rank) + 32 * quarter;   // this warp's first row within the tile
+      const int li = li0 + lane;
+      const bool valid = li < nrows;
+      const int64_t row0 = static_cast<int64_t>(p.tile_row0[t]) + li0;   // plan row of lane 0
+      const float scale = p.st_a[0] * p.st_b[e];
+      if (!__all_sync(0xffffffffu, mbar_wait_cluster(accf_bar, done & 1, abort_flag))) break;
+      tc_fence_after();
+      // packed bf16 outputs of this lane's row: gate/up 64 h values (columns
+      // 128 j + 64 half ..), down 128 y values (columns 256 j + 128 half ..)
+      constexpr int NW = GATEUP ? 32 : 64;
+      uint32_t packed[NW];
+      uint32_t hmax = 0u;
+      if (GATEUP) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t g[32], u[32];
+          tc_ld_32cols(tmem + lanes + static_cast<uint32_t>(64 * half + 32 * c), g);
+          tc_ld_32cols(tmem + lanes + static_cast<uint32_t>(128 + 64 * half + 32 * c), u);
+          tc_wait_ld();
+          if (c == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acce_bar, 0);
+          }
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float g0 = __uint_as_float(g[2 * q]) * scale, g1 = __uint_as_float(g[2 * q + 1]) * scale;
+            const float u0 = __uint_as_float(u[2 * q]) * scale, u1 = __uint_as_float(u[2 * q + 1]) * scale;
+            const uint32_t b = f32x2_to_bf16x2(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
+                                               __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+            packed[16 * c + q] = b;
+            hmax = max(hmax, max(b & 0x7FFFu, (b >> 16) & 0x7FFFu));
+          }
+        }
+        const uint32_t m = __reduce_max_sync(0xffffffffu, valid ? hmax : 0u);
+        if (lane == 0 && m != 0u) atomicMax(p.amax_bits, m << 16);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tc_ld_32cols(tmem + lanes + static_cast<uint32_t>(half * 128 + 32 * c), r);
+          tc_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            packed[16 * c + q] = f32x2_to_bf16x2(__uint_as_float(r[2 * q]) * scale, __uint_as_float(r[2 * q + 1]) * scale);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acce_bar, 0);
+      }
+      const int col0 = GATEUP ? 128 * j + 64 * half : 256 * j + 128 * half;
+      if (li0 + 32 <= nrows) {
+        // 64-column boxes through this warp's staging buffer (128B swizzle:
+        // 16-byte chunk c of row r at r * 128 + (c ^ (r % 8)) * 16)
+#pragma unroll
+        for (int b = 0; b < NW / 32; ++b) {
+          // the previous box's store has finished reading the staging buffer
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t a = stage_out + lane * 128 + ((c ^ (lane & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(packed[32 * b + 4 * c]),
+                         "r"(packed[32 * b + 4 * c + 1]), "r"(packed[32 * b + 4 * c + 2]),
+                         "r"(packed[32 * b + 4 * c + 3])
+                         : "memory");
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the tensor store
+          __syncwarp();
+          if (lane == 0) {
+            asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(&map_out),
+                         "r"(col0 + 64 * b), "r"(static_cast<int>(row0)), "r"(stage_out)
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+        }
+      } else if (valid) {
+        // the tile's ragged last rows: plain stores of this lane's row
+        uint4* dst = reinterpret_cast<uint4*>((GATEUP ? p.h_out + (row0 + lane) * p.inter
+                                                      : p.y_out + (row0 + lane) * p.hidden) + col0);
+#pragma unroll
+        for (int q = 0; q < NW / 4; ++q)
+          dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+      }
+    }
+    // stores complete before the CTA exits
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+  } else {
+    // scale warps: this CTA's A scales and the whole weight block's scales
+    // into its own tensor memory (layout as in gemm_w4a4_kernel), then tell
+    // the even CTA
+    const uint32_t lane_cols = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + SF_TMEM_BASE;
+    int it = 0;
+    for (int w = pair_id; w < n_work; w += n_pairs) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      bool ok = true;
+      for (int ks = 0; ks < n_k; ++ks, ++it) {
+        const int s = it % P_STAGES;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait_bounded(full_bar(s), (it / P_STAGES) & 1, abort_flag, &g_device_status))) {
+          ok = false;
+          break;
+        }
+        uint32_t v[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 x = lds128(stage_sfa(s) + 512 * k + 16 * lane);
+          v[4 * k] = x.x, v[4 * k + 1] = x.y, v[4 * k + 2] = x.z, v[4 * k + 3] = x.w;
+        }
+        const uint32_t col = lane_cols + s * SF_COLS_PER_STAGE;
+        tc_st_16cols(col, v);
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint4 x = lds128(stage_sfb(s) + 2048 * h + 512 * (2 * pr + kk) + 16 * lane);
+              const int o = 8 * kk + 4 * h;
+              v[o] = x.x, v[o + 1] = x.y, v[o + 2] = x.z, v[o + 3] = x.w;
+            }
+          tc_st_16cols(col + 16 + 16 * pr, v);
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(ready_bar(s), 0);
+      }
+      if (!ok) break;
+    }
+  }
+
+  // Unwind: copies and MMAs already issued land (bounded) before the memory they target goes away.
+  if (prod >= 0 && lane == 0 && *abort_flag) {
+    for (int it = next_it - 1; it >= 0 && it >= next_it - 2 * P_STAGES; --it)
+      if ((it & 1) == prod)
+        mbar_wait_bounded(full_bar(it % P_STAGES), (it / P_STAGES) & 1, nullptr, &g_device_status, 100000000ull);
+  }
+  if (warp == 1 && rank == 0 && lane == 0 && *abort_flag && mma_tiles > 0) {
+    mbar_wait_bounded(accf_bar, (mma_tiles - 1) & 1, nullptr, &g_device_status, 100000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // the peer is done with this CTA's shared and tensor memory
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
 }  // namespace
 
 int launch_gemm_w4a4(const nvfp4_tensor_t& A, const nvfp4_tensor_t& W, uint16_t* Y, void* ws,
@@ -1283,12 +1592,19 @@ int read_device_status(int* out, cudaStream_t stream) {
 int launch_grouped_w4a4(bool gateup, const uint8_t* a_codes, const uint8_t* a_scales, const float* st_a,
                         int64_t a_rows, const nvfp4_tensor_t& W, const int* tile_count, const int* tile_expert,
                         const int* tile_row0, const int* tile_rows, int64_t max_tiles, int inter, int hidden,
-                        uint16_t* h_out, unsigned int* amax_bits, uint16_t* y_out, cudaStream_t stream) {
+                        uint16_t* h_out, unsigned int* amax_bits, uint16_t* y_out, int64_t out_rows, bool pair,
+                        cudaStream_t stream) {
   const int64_t K = W.K, rows = static_cast<int64_t>(W.batch) * W.rows;
-  CUtensorMap map_a, map_b;
+  CUtensorMap map_a, map_b, map_out;
   int rc = make_tmap_2d_u8(&map_a, a_codes, K / 2, a_rows, K / 2, 128, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != NVFP4_OK) return rc;
   rc = make_tmap_2d_u8(&map_b, W.codes, K / 2, rows, K / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != NVFP4_OK) return rc;
+  // the output rows in the plan's order, 32-row x 64-column boxes
+  rc = gateup ? make_tmap_2d_u16(&map_out, h_out, inter, out_rows, static_cast<int64_t>(inter) * 2, 64, 32,
+                                 CU_TENSOR_MAP_SWIZZLE_128B)
+              : make_tmap_2d_u16(&map_out, y_out, hidden, out_rows, static_cast<int64_t>(hidden) * 2, 64, 32,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != NVFP4_OK) return rc;
   GroupedW4A4Params p{};
   p.sfa = a_scales;
@@ -1308,19 +1624,34 @@ int launch_grouped_w4a4(bool gateup, const uint8_t* a_codes, const uint8_t* a_sc
   p.h_out = h_out;
   p.amax_bits = amax_bits;
   p.y_out = y_out;
-  // persistent: at most one CTA per SM, fewer when the plan cannot have that many work items
   const int64_t work_max = max_tiles * p.n_tiles;
-  const unsigned grid = static_cast<unsigned>(work_max < sm_count() ? work_max : sm_count());
-  if (gateup) {
-    rc = ensure_smem(grouped_w4a4_kernel<true>, SMEM_BYTES);
-    if (rc != NVFP4_OK) return rc;
-    grouped_w4a4_kernel<true><<<grid, THREADS, SMEM_BYTES, stream>>>(map_a, map_b, p);
-  } else {
-    rc = ensure_smem(grouped_w4a4_kernel<false>, SMEM_BYTES);
-    if (rc != NVFP4_OK) return rc;
-    grouped_w4a4_kernel<false><<<grid, THREADS, SMEM_BYTES, stream>>>(map_a, map_b, p);
+  if (!pair) {
+    // persistent: at most one CTA per SM, fewer when the plan cannot have that many work items
+    const unsigned grid = static_cast<unsigned>(work_max < sm_count() ? work_max : sm_count());
+    if (gateup) {
+      rc = ensure_smem(grouped_w4a4_kernel<true>, SMEM_BYTES);
+      if (rc != NVFP4_OK) return rc;
+      grouped_w4a4_kernel<true><<<grid, THREADS, SMEM_BYTES, stream>>>(map_a, map_b, p);
+    } else {
+      rc = ensure_smem(grouped_w4a4_kernel<false>, SMEM_BYTES);
+      if (rc != NVFP4_OK) return rc;
+      grouped_w4a4_kernel<false><<<grid, THREADS, SMEM_BYTES, stream>>>(map_a, map_b, p);
+    }
+    return from_cuda(cudaGetLastError());
   }
-  return from_cuda(cudaGetLastError());
+  // persistent CTA pairs: at most one CTA per SM, fewer when the plan cannot have that many work items
+  const int64_t pairs_max = sm_count() / 2;
+  const unsigned grid = static_cast<unsigned>(2 * (work_max < pairs_max ? work_max : pairs_max));
+  if (gateup) {
+    rc = ensure_smem(grouped_w4a4_pair_kernel<true>, P_SMEM_BYTES);
+    if (rc != NVFP4_OK) return rc;
+    return launch_ex(grouped_w4a4_pair_kernel<true>, dim3(grid), dim3(THREADS), P_SMEM_BYTES, 2, false, stream,
+                     map_a, map_b, map_out, p);
+  }
+  rc = ensure_smem(grouped_w4a4_pair_kernel<false>, P_SMEM_BYTES);
+  if (rc != NVFP4_OK) return rc;
+  return launch_ex(grouped_w4a4_pair_kernel<false>, dim3(grid), dim3(THREADS), P_SMEM_BYTES, 2, false, stream,
+                   map_a, map_b, map_out, p);
 }
 
 int probe_fp4_mma_rate(int n_mma, int n_ctas, cudaStream_t stream) {

@@ -124,10 +124,15 @@ int read_device_status(int* out, cudaStream_t stream);
 int selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream);
 int probe_fp4_mma_rate(int n_mma, int n_ctas, cudaStream_t stream);
 // Grouped W4A4 expert GEMM over a routing plan's tile table (gate/up with
-// SiLU * mul, or down); a_codes / a_scales: tile-major routed rows [a_rows][K].
+// SiLU * mul, or down): with `pair`, CTA pairs over tiles of up to W4A4_TILE
+// routed rows, else one CTA per tile of up to 128; a_codes / a_scales:
+// tile-major routed rows [a_rows][K] (tile t at rows t * tile size);
+// h_out / y_out: [out_rows] rows in the plan's order.
+constexpr int W4A4_TILE = 256;
 int launch_grouped_w4a4(bool gateup, const uint8_t* a_codes, const uint8_t* a_scales, const float* st_a,
                         int64_t a_rows, const nvfp4_tensor_t& W, const int* tile_count, const int* tile_expert,
                         const int* tile_row0, const int* tile_rows, int64_t max_tiles, int inter, int hidden,
-                        uint16_t* h_out, unsigned int* amax_bits, uint16_t* y_out, cudaStream_t stream);
+                        uint16_t* h_out, unsigned int* amax_bits, uint16_t* y_out, int64_t out_rows, bool pair,
+                        cudaStream_t stream);
 
 }  // namespace nvfp4

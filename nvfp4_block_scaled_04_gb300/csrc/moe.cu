@@ -129,6 +129,10 @@ constexpr int PLAN_COOP_SLICE = 512;
 constexpr int PLAN_COOP_THREADS = 512;
 constexpr int PLAN_COOP_MAX_E = 256;
 
+// rows of the W4A4 layer's tile-major matrices: every tile of up to
+// W4A4_TILE routed rows of one expert in its own W4A4_TILE rows
+inline int64_t w4a4_tile_rows(int64_t R, int64_t E) { return (ceil_div(R, W4A4_TILE) + E) * W4A4_TILE; }
+
 struct MoeWs {
   int* chunk_count;   // [1]
   int* poff;          // [E]
@@ -149,7 +153,7 @@ struct MoeWs {
   uint4* xfrag2;      // h, K = I
   uint16_t* ybuf;     // [padded rows][H] bf16: each routed row's expert output
   // W4A4 layer: the routed rows as NVFP4 in tile-major order (tile t = rows
-  // [128 t, 128 t + 128)), codes and MMA-layout scales, for x and for h
+  // [W4A4_TILE t, W4A4_TILE (t + 1))), codes and MMA-layout scales, for x and h
   uint8_t* xq_codes;
   uint8_t* xq_scales;
   uint8_t* xt_codes;   // the layer input quantised once per token: [T][H/2]
@@ -200,7 +204,7 @@ MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
   if (!w4a4) w.xfrag2 = reinterpret_cast<uint4*>(take(xfrag_bytes(w.max_chunks, I)));
   w.ybuf = reinterpret_cast<uint16_t*>(take(static_cast<size_t>(rows) * H * sizeof(uint16_t)));
   if (w4a4) {
-    const size_t trows = static_cast<size_t>(w.max_tiles) * 128;
+    const size_t trows = static_cast<size_t>(w4a4_tile_rows(R, E));
     w.xt_codes = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * H / 2));
     w.xt_scales = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(T) * H / 16));
     w.q_ws = take(quantize_workspace_bytes());
@@ -217,16 +221,17 @@ MoeWs carve_moe(void* base, int64_t T, int64_t H, int64_t I, int64_t E, int64_t 
 
 // The routed rows of the layer input in tile-major NVFP4 (the W4A4 gate/up
 // GEMM's A operand), copied from the tokens' rows quantised once: one warp
-// per row r = 128 t + i of tile t; rows i < tile_rows[t] get their token's
+// per row r = tile t' + i of tile t (tile rows per tile: 128 or W4A4_TILE);
+// rows i < tile_rows[t] get their token's
 // codes (K/2 bytes) and block scales (re-laid into the MMA layout, four
 // scale columns per 32-bit store), the rest of the tile zeros.
 __global__ void __launch_bounds__(8 * 32) gather_routed_kernel(const uint8_t* codes_in, const uint8_t* scales_in,
                                                                int64_t K, const int* row_of, const int* tile_count,
                                                                const int* tile_row0, const int* tile_rows,
-                                                               uint8_t* codes, uint8_t* scales) {
+                                                               uint8_t* codes, uint8_t* scales, int tile) {
   const int lane = threadIdx.x & 31;
   const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int t = static_cast<int>(r >> 7), i = static_cast<int>(r & 127);
+  const int t = static_cast<int>(r / tile), i = static_cast<int>(r % tile);
   if (t >= *tile_count) return;
   int tok = -1;
   if (i < tile_rows[t]) tok = row_of[static_cast<int64_t>(tile_row0[t]) + i];
@@ -241,7 +246,8 @@ __global__ void __launch_bounds__(8 * 32) gather_routed_kernel(const uint8_t* co
 }
 
 // NVFP4 of the routed rows in tile-major order (the W4A4 expert GEMMs' A
-// operand): one warp per row r = 128 t + i of tile t; rows i < tile_rows[t]
+// operand): one warp per row r = tile t + i of tile t (128 or W4A4_TILE rows
+// per tile); rows i < tile_rows[t]
 // hold routed row tile_row0[t] + i of the plan (gather: its token's row of
 // src; else that row of src), the rest of the tile zero codes and scales.
 // The tensor scale is s_t = amax / 2688 (1 if amax is 0), written to
@@ -251,10 +257,10 @@ __global__ void __launch_bounds__(QR_WARPS * 32) quantize_routed_kernel(const ui
                                                                          const int* row_of, const int* tile_count,
                                                                          const int* tile_row0, const int* tile_rows,
                                                                          const unsigned int* amax_bits, float* s_t_out,
-                                                                         uint8_t* codes, uint8_t* scales) {
+                                                                         uint8_t* codes, uint8_t* scales, int tile) {
   const int lane = threadIdx.x & 31;
   const int64_t r = static_cast<int64_t>(blockIdx.x) * QR_WARPS + (threadIdx.x >> 5);
-  const int t = static_cast<int>(r >> 7), i = static_cast<int>(r & 127);
+  const int t = static_cast<int>(r / tile), i = static_cast<int>(r % tile);
   if (t >= *tile_count) return;
   const float amax = __uint_as_float(*amax_bits);
   const float st = amax > 0.f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
@@ -918,8 +924,13 @@ int launch_grouped_gemm_w4a4(const uint16_t* X, int64_t T, int topk, const int32
   const int64_t R = T * topk;
   if (E > PLAN_MAX_E || R >= (1LL << 31)) return NVFP4_ERR_UNSUPPORTED_SHAPE;   // plan positions are int
   const MoeWs m = carve_moe(ws, T, H, I, E, topk, true);
-  if (m.max_tiles * 128 >= (1LL << 31) / (H / 2)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  int rc = launch_route_plan(ids, R, topk, E, m, PLAN_TILE_MIN, stream);
+  // experts with 256+ routed rows on average: CTA pairs over 256-row tiles;
+  // fewer: one CTA per 128-row tile (a pair's 256 rows would be mostly padding)
+  const bool pair = R >= static_cast<int64_t>(W4A4_TILE) * E;
+  const int tile = pair ? W4A4_TILE : PLAN_TILE_MIN;
+  const int64_t trows = (ceil_div(R, tile) + E) * tile;   // <= w4a4_tile_rows(R, E), the buffers' rows
+  if (trows >= (1LL << 31) / (H / 2)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  int rc = launch_route_plan(ids, R, topk, E, m, tile, stream);
   if (rc != NVFP4_OK) return rc;
   // the layer input quantised once per token (dynamic tensor scale), then its
   // routed rows gathered into the tile-major matrix
@@ -927,24 +938,23 @@ int launch_grouped_gemm_w4a4(const uint16_t* X, int64_t T, int topk, const int32
                        NVFP4_SCALES_ROWMAJOR, m.q_ws, stream);
   if (rc != NVFP4_OK) return rc;
   if (cudaMemsetAsync(m.amax + 1, 0, sizeof(unsigned int), stream) != cudaSuccess) return NVFP4_ERR_CUDA;
-  const int64_t trows = m.max_tiles * 128;
   const unsigned qgrid = static_cast<unsigned>(trows / QR_WARPS);
   gather_routed_kernel<<<qgrid, 8 * 32, 0, stream>>>(m.xt_codes, m.xt_scales, H, m.row_of, m.tile_count, m.tile_row0,
-                                                     m.tile_rows, m.xq_codes, m.xq_scales);
+                                                     m.tile_rows, m.xq_codes, m.xq_scales, tile);
   rc = from_cuda(cudaGetLastError());
   if (rc != NVFP4_OK) return rc;
   rc = launch_grouped_w4a4(true, m.xq_codes, m.xq_scales, m.st, trows, W13, m.tile_count, m.tile_expert, m.tile_row0,
                            m.tile_rows, m.max_tiles, static_cast<int>(I), static_cast<int>(H), m.hbuf, m.amax + 1,
-                           nullptr, stream);
+                           nullptr, m.max_chunks * GV_MCHUNK, pair, stream);
   if (rc != NVFP4_OK) return rc;
   quantize_routed_kernel<<<qgrid, QR_WARPS * 32, 0, stream>>>(m.hbuf, I, false, m.row_of, m.tile_count, m.tile_row0,
                                                               m.tile_rows, m.amax + 1, m.st + 1, m.hq_codes,
-                                                              m.hq_scales);
+                                                              m.hq_scales, tile);
   rc = from_cuda(cudaGetLastError());
   if (rc != NVFP4_OK) return rc;
   rc = launch_grouped_w4a4(false, m.hq_codes, m.hq_scales, m.st + 1, trows, W2, m.tile_count, m.tile_expert,
                            m.tile_row0, m.tile_rows, m.max_tiles, static_cast<int>(I), static_cast<int>(H), nullptr,
-                           nullptr, m.ybuf, stream);
+                           nullptr, m.ybuf, m.max_chunks * GV_MCHUNK, pair, stream);
   if (rc != NVFP4_OK) return rc;
   return combine(m, w, T, topk, H, out, stream);
 }

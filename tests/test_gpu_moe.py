@@ -219,8 +219,11 @@ def ref_w4a4(x, w13, w2, ids, wts):
                               [O.quantize(t.numpy()) for t in w13], [O.quantize(t.numpy()) for t in w2])
 
 
+# the last three: 256+ routed rows per expert on average, so the expert GEMMs
+# run on CTA pairs over 256-row tiles (ragged tiles included)
 @pytest.mark.parametrize("T,E,H,I,k", [(64, 4, 256, 128, 2), (300, 8, 512, 256, 3), (37, 16, 256, 384, 8),
-                                       (1, 4, 256, 128, 1), (700, 4, 256, 256, 2)])
+                                       (1, 4, 256, 128, 1), (700, 4, 256, 256, 2), (1024, 4, 256, 256, 2),
+                                       (700, 2, 256, 384, 1), (2048, 8, 512, 256, 2)])
 def test_w4a4_layers(T, E, H, I, k):
     """Ragged tiles (several 128-row tiles per expert, ragged tails), one
     token, top-8, I not a multiple of 256 (three-atom last K stage)."""
@@ -230,12 +233,14 @@ def test_w4a4_layers(T, E, H, I, k):
     assert O.rel_fro(out, ref_w4a4(x, w13, w2, ids, wts)) <= TOL
 
 
-def test_w4a4_skewed_routing_and_determinism():
-    """600 rows on one expert (five tiles, the last of 88 rows), the others
-    empty; two calls give identical bits."""
-    T, E, H, I = 600, 4, 256, 256
+@pytest.mark.parametrize("E", [4, 2])
+def test_w4a4_skewed_routing_and_determinism(E):
+    """600 rows on one expert, the others empty; two calls give identical bits.
+    E = 4: one-CTA kernels, five 120-row tiles; E = 2 (300 rows per expert on
+    average): CTA pairs, three 200-row tiles, each with a ragged odd half."""
+    T, H, I = 600, 256, 256
     logits, x, w13, w2 = moe_case(T, E, H, I, 1, seed=41)
-    ids = torch.full((T, 1), 2, dtype=torch.int32, device=DEV)
+    ids = torch.full((T, 1), E - 1, dtype=torch.int32, device=DEV)
     wts = torch.full((T, 1), 0.75, device=DEV)
     a = run_gpu_w4a4(x, w13, w2, ids, wts)
     b = run_gpu_w4a4(x, w13, w2, ids, wts)
