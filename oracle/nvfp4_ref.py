@@ -25,7 +25,7 @@ What it computes, and the passages it follows
   mask cannot alter what the model emits (Serving Qwen3.8-27B..., "The masked
   head trick").
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   R1 tensor scale  s_t = amax(|x|) / 2688 in fp32 (2688 = 6 * 448); s_t = 1
      when the tensor is all zeros.
   R2 block scale   d = fp32(s_t * 6); sb = fp32(amax_block / d);
