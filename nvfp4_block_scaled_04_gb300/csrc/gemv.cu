@@ -15,15 +15,17 @@ namespace {
 // completion counter) of the kernel that follows.
 // 1024 threads per row: up to K = 32768 the row is read once, into registers.
 // Launched as a programmatic dependent of whatever kernel precedes it on the
-// stream: it lets its own GEMV launch at once (that GEMV starts streaming its
-// weights) and then waits for the preceding kernel to finish before it
-// touches memory - which may be that kernel's output, or a workspace it uses.
+// stream, so it is resident and waiting while that kernel drains. Once that
+// kernel has finished (its writes visible) it lets its own GEMV launch, which
+// starts streaming its weights (and reading the index of gathered rows)
+// while this kernel converts the activations: everything enqueued before the
+// call is complete before the GEMV reads any of its inputs.
 constexpr int XPREP_THREADS = 1024;
 __global__ void __launch_bounds__(XPREP_THREADS) xprep_dense_kernel(const uint16_t* X, int64_t M, int64_t K,
                                                                      uint4* xfrag, int* pexp,
                                                                      unsigned int* counters, int n_counters) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   if (blockIdx.x == 0 && blockIdx.y == 0)
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0u;
   const int64_t out_row = static_cast<int64_t>(blockIdx.y) * GV_MCHUNK + blockIdx.x;
@@ -97,12 +99,15 @@ int launch_tma_plain_nt(const TmaSkinnyParams& p, const CUtensorMap& mc, const C
 
 // GEMV with argmax on the TMA-fed kernel (split 1). With an index the codes
 // and scales come in by tile::gather4 of one-row-high boxes (GATHER), over
-// the whole weight by 2-D boxes of 128 rows.
+// the whole weight by 2-D boxes of 128 rows. The plain GEMV's warp layout at
+// every token count: a row's logit is summed in the order the unsplit GEMV
+// sums that output, so its bits do not depend on the batch, and rounded to
+// bf16 it is the GEMV's output for that row.
 template <int NT, bool GATHER>
 int launch_tma_argmax_nt(const TmaSkinnyParams& p, const CUtensorMap& mc, const CUtensorMap& ms, dim3 grid,
                          cudaStream_t stream) {
-  constexpr int MT = NT >= 2 ? 2 : 1;
-  constexpr int KW = NT >= 2 ? 2 : 1;
+  constexpr int MT = 2;
+  constexpr int KW = 2;
   using C = GtCfg<NT, GATHER ? GT_SCALES_GATHERED : GT_SCALES>;
   auto k = skinny_tma_kernel<NT, SK_ARGMAX, MT, KW, GATHER>;
   int rc = ensure_smem(k, C::SMEM);

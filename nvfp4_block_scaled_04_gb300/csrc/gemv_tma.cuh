@@ -54,7 +54,7 @@ struct GtCfg {
   static constexpr int STAGE = (GT_CODES + SC + XB + 1023) / 1024 * 1024;
   static constexpr int STAGES = NT <= 2 ? 4 : 3;
   static constexpr int RING = STAGES * STAGE;
-  static constexpr int SMEM = RING + 1024 /*alignment*/ + 512 /*barriers, shifts, flags*/;
+  static constexpr int SMEM = RING + 1024 /*alignment*/ + 1024 /*barriers, shifts, flags, argmax ids*/;
 };
 
 struct TmaSkinnyParams {
@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ring_ptr + C::RING + 64 + 128);
   int* s_last = reinterpret_cast<int*>(ring_ptr + C::RING + 64 + 132);
   unsigned long long* kbest = reinterpret_cast<unsigned long long*>(ring_ptr + C::RING + 256);   // ARGMAX, [32]
+  int* sidx = reinterpret_cast<int*>(ring_ptr + C::RING + 512);   // ARGMAX: vocabulary ids of the tile's rows, [128]
   static_assert(2 * C::STAGES * 8 <= 64, "barrier area");
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (C::STAGES + s); };
@@ -376,6 +377,11 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
       }
     }
   } else {
+    if (MODE == SK_ARGMAX && tid < GV_ROWS) {
+      // the epilogue's row ids, fetched while the first stages are in flight
+      const int64_t j = row_tile * GV_ROWS + tid;
+      sidx[tid] = j < p.n_rows ? (p.idx ? p.idx[j] : static_cast<int>(j)) : 0;
+    }
     const int sw = gt_sigma(g);               // smem row (mod 8) of MMA row g
     const int grp = warp % NGR;               // row group of this warp
     const int jk = warp / NGR;                // its K-iteration within a stage when KW == 2
@@ -446,7 +452,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
           // key: logit order first, then the lower vocabulary id
           const int64_t j = row_tile * GV_ROWS + r;
           if (j < p.n_rows) {
-            const uint32_t vid = p.idx ? static_cast<uint32_t>(p.idx[j]) : static_cast<uint32_t>(j);
+            const uint32_t vid = static_cast<uint32_t>(sidx[r]);
             key = (static_cast<unsigned long long>(float_order_key(v * mul)) << 32) | (0xFFFFFFFFu - vid);
           }
           key_tok = tok;   // set for rows past the end too: the groups below follow the output index

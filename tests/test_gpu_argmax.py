@@ -52,6 +52,35 @@ def test_identity_index_equals_full_and_repeat_calls_agree():
     assert torch.equal(a[0], b[0]) and torch.equal(a[0], c[0]) and torch.equal(a[1], c[1])
 
 
+def test_compact_head_bits_match_plain_decode():
+    """Every fast path gated byte-identical to plain decode (Serving
+    Qwen3.8-27B..., "Rules I learned the expensive way"), for the draft head
+    on compact rows: at 32,768 rows x 5120 (256 row tiles, one GEMV pass
+    without split-K) a token's winning logit rounded to bf16 is the plain
+    GEMV's largest output and the winner's own output, and the token's id and
+    logit bits are the same alone and inside batches of 5, 8, 9 and 32."""
+    m = nv()
+    V, N, K = 248320, 32768, 5120
+    qw = m.quantize(synth.normal_f32((N, K), 0.02, seed=61).to(DEV))
+    ids = synth.permutation_prefix(V, N, seed=62).to(DEV)
+    pos = torch.full((V,), -1, dtype=torch.int64, device=DEV)
+    pos[ids.long()] = torch.arange(N, device=DEV)
+    tok = synth.normal_bf16((1, K), seed=63).to(DEV)
+    seen = []
+    for M in (1, 5, 8, 9, 32):
+        x = synth.normal_bf16((M, K), seed=M + 300).to(DEV)
+        x[M - 1] = tok[0]
+        wid, logit = m.gemv_argmax(x, qw, ids)
+        y = m.gemm_w4a16(x, qw).float()
+        best = y.max(dim=1).values
+        assert torch.equal(logit.to(torch.bfloat16).float(), best), M
+        rows = pos[wid.long()]
+        assert bool((rows >= 0).all())
+        assert torch.equal(y[torch.arange(M, device=DEV), rows], best), M
+        seen.append((int(wid[M - 1]), int(logit[M - 1:M].view(torch.int32)[0])))
+    assert all(s == seen[0] for s in seen), seen
+
+
 def test_planted_winner():
     m = nv()
     V, K = 5000, 256
