@@ -22,6 +22,13 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t mma_scale_rows(int64_t rows) { return ceil_div(rows, 128) * 128; }
 inline int64_t mma_scale_cols(int64_t K) { return ceil_div(K / 16, 4) * 4; }
 
+// GPU-scope acquire-release fence for the last-arrival reductions: a
+// thread's global writes before it are visible to any thread that observes
+// (through the arrival counter) a write of this CTA after it, and reads
+// after it see every write published that way before the counter value
+// this CTA observed.
+NVFP4_DEV void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // ------------------------------------------------------------ conversions
 
 // Eight packed e2m1 codes -> four f16x2 words (byte b -> out[b]); the low

@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(GV_THREADS, 2) skinny_kernel(const SkinnyParam
   if (MODE == SK_ARGMAX) {
     __syncthreads();
     if (tid < rows_in_chunk) atomicMax(&p.keys[row_base + tid], kbest[tid]);
-    __threadfence();
+    fence_acq_rel_gpu();
     __syncthreads();
     if (tid == 0) {
       const unsigned int total = gridDim.x * gridDim.y * gridDim.z;
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(GV_THREADS, 2) skinny_kernel(const SkinnyParam
     }
     __syncthreads();
     if (s_last) {
-      __threadfence();
+      fence_acq_rel_gpu();
       for (int64_t m = tid; m < p.M; m += GV_THREADS) {
         const unsigned long long key = atomicExch(&p.keys[m], 0ull);
         p.out_ids[m] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));

@@ -488,12 +488,12 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
       // finish reads them out and leaves keys and counter at zero
       __syncthreads();
       if (tid < rows_in_chunk) atomicMax(&p.keys[row_base + tid], kbest[tid]);
-      __threadfence();
+      fence_acq_rel_gpu();
       __syncthreads();
       if (tid == 0) *s_last = atomicAdd(p.counter, 1u) == gridDim.x * gridDim.y * gridDim.z - 1;
       __syncthreads();
       if (*s_last) {
-        __threadfence();
+        fence_acq_rel_gpu();
         for (int64_t m = tid; m < p.M; m += NTHR) {
           const unsigned long long key = atomicExch(&p.keys[m], 0ull);
           p.out_ids[m] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
@@ -523,14 +523,14 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
       const int tok = e4 >> 5, r = (e4 & 31) * 4;
       mine[e4] = make_float4(psum(tok, r), psum(tok, r + 1), psum(tok, r + 2), psum(tok, r + 3));
     }
-    __threadfence();
+    fence_acq_rel_gpu();
     __syncthreads();
     if (tid == 0) *s_last = atomicAdd(&p.counters[tile], 1u) == static_cast<unsigned>(S - 1);
     __syncthreads();
     if (MODE == SK_GATEUP_DENSE && *s_last) {
       // gate rows r .. r + 3 are float4 group tok * 32 + r / 4, the matching
       // up rows group tok * 32 + 16 + r / 4; both summed in split order
-      __threadfence();
+      fence_acq_rel_gpu();
       const float4* all = reinterpret_cast<const float4*>(p.partials) + tile * S * P4;
       const int n4g = rows_in_chunk * 16;
       for (int e = tid; e < n4g; e += NTHR) {
@@ -559,7 +559,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
             make_uint2(f32x2_to_bf16x2(h4[0], h4[1]), f32x2_to_bf16x2(h4[2], h4[3]));
       }
     } else if (*s_last) {
-      __threadfence();
+      fence_acq_rel_gpu();
       const float4* all = reinterpret_cast<const float4*>(p.partials) + tile * S * P4;
       // two groups per thread per round, all S (<= 8) partials of both requested before any
       // is summed: the reduction costs one or two L2 round trips, not one per output
@@ -778,12 +778,12 @@ static __global__ void __launch_bounds__(RS_THREADS, 1)
   // reads them out and leaves keys and counter at zero
   const int rows_in_chunk = static_cast<int>(p.M);
   if (tid < rows_in_chunk) atomicMax(&p.keys[tid], kbest[tid]);
-  __threadfence();
+  fence_acq_rel_gpu();
   __syncthreads();
   if (tid == 0) *s_last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
   __syncthreads();
   if (*s_last) {
-    __threadfence();
+    fence_acq_rel_gpu();
     for (int64_t m = tid; m < p.M; m += RS_THREADS) {
       const unsigned long long key = atomicExch(&p.keys[m], 0ull);
       p.out_ids[m] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key));
