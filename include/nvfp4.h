@@ -19,7 +19,10 @@
  *  - Pointers are DEVICE pointers unless stated otherwise; the caller owns
  *    every buffer. The library allocates nothing.
  *  - Calls are asynchronous on `stream` (0 = legacy default stream); nothing
- *    synchronises the host.
+ *    synchronises the host. Stream order holds for every input: a call
+ *    reads nothing before the work enqueued ahead of it has finished. The
+ *    decode entry points overlap a call's start with the previous kernel's
+ *    drain (programmatic dependent launch) only in ways that keep this true.
  *  - Return value: NVFP4_OK (0) or a negative NVFP4_ERR_*; arguments are
  *    validated on the host before anything is launched, so an error return
  *    means nothing was enqueued (except NVFP4_ERR_CUDA, raised by a failed
