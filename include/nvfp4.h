@@ -281,7 +281,10 @@ int nvfp4_grouped_gemm_w4a4(const void* X, int64_t T, int topk, const int32_t* t
  *   out_ids[m]  = idx[argmax_j logit[m][j]], ties to the lowest vocabulary id
  *   out_logit[m] = that maximum logit (fp32), if out_logit != NULL.
  *   H      device bf16 [M][K];  W  NVFP4 [V][K], batch 1, ROWMAJOR;
- *   idx    device int32 [n_idx], each in [0, V); NULL = every row (n_idx = V)
+ *   idx    device int32 [n_idx]; NULL = every row (n_idx = V). An entry
+ *          outside [0, V) is skipped: that row is never read and never
+ *          reported; if no entry is valid, out_ids[m] = -1 and out_logit[m]
+ *          is a NaN.
  *   workspace >= nvfp4_workspace_size(NVFP4_OP_GATHER_ARGMAX, M, n_idx, K, 0, 0).
  * K must be a multiple of 128; 1 <= M <= 32; n_idx >= 1. */
 int nvfp4_gather_gemv_argmax(const void* H, int64_t M, nvfp4_tensor_t W,

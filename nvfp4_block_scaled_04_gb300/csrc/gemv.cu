@@ -352,6 +352,7 @@ int launch_gather_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, 
     q.split = 1;
     q.status = device_status_ptr();
     q.idx = idx;
+    q.w_rows = W.rows;
     q.keys = w.keys;
     q.counter = w.counter;
     q.out_ids = out_ids;
@@ -382,6 +383,7 @@ int launch_gather_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, 
     q.split = 1;
     q.status = device_status_ptr();
     q.idx = idx;
+    q.w_rows = W.rows;
     q.keys = w.keys;
     q.counter = w.counter;
     q.out_ids = out_ids;
@@ -409,6 +411,7 @@ int launch_gather_argmax(const uint16_t* H, int64_t M, const nvfp4_tensor_t& W, 
   p.K = K;
   p.n_rows = n_idx;
   p.idx = idx;
+  p.w_rows = W.rows;
   p.xfrag = w.xfrag;
   p.pexp = w.pexp;
   p.M = M;

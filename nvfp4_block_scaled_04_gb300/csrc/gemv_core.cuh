@@ -235,6 +235,7 @@ struct SkinnyParams {
   int64_t K;
   int64_t n_rows;              // PLAIN: N; ARGMAX: number of candidate rows
   const int32_t* idx;          // ARGMAX: candidate -> vocabulary row (nullable)
+  int64_t w_rows;              // ARGMAX: rows of the weight; an idx entry outside [0, w_rows) is skipped
   // activations in fragment layout and their per-row power-of-two shifts
   const uint4* xfrag;
   const int* pexp;
@@ -301,6 +302,7 @@ __global__ void __launch_bounds__(GV_THREADS, 2) skinny_kernel(const SkinnyParam
     } else if (MODE == SK_ARGMAX) {
       const int64_t j = row_tile * GV_ROWS + r;
       w = j < p.n_rows ? (p.idx ? static_cast<int64_t>(p.idx[j]) : j) : 0;
+      if (w < 0 || w >= p.w_rows) w = 0;   // a skipped entry reads row 0; its key is dropped below
     } else if (MODE == SK_MOE_GATEUP) {
       const int64_t rr = r < 64 ? row_tile * 64 + r : p.inter + row_tile * 64 + (r - 64);
       w = expert * p.rows_per_expert + rr;
@@ -356,8 +358,9 @@ __global__ void __launch_bounds__(GV_THREADS, 2) skinny_kernel(const SkinnyParam
       if (n < p.n_rows) p.Y[(row_base + tok) * p.n_rows + n] = static_cast<uint16_t>(f32_to_bf16_bits(v * mul));
     } else if (MODE == SK_ARGMAX) {
       const int64_t j = row_tile * GV_ROWS + r;
-      if (j < p.n_rows) {
-        const uint32_t vid = p.idx ? static_cast<uint32_t>(p.idx[j]) : static_cast<uint32_t>(j);
+      const int64_t vj = j < p.n_rows ? (p.idx ? static_cast<int64_t>(p.idx[j]) : j) : -1;
+      if (vj >= 0 && vj < p.w_rows) {
+        const uint32_t vid = static_cast<uint32_t>(vj);
         const unsigned long long key =
             (static_cast<unsigned long long>(float_order_key(v * mul)) << 32) | (0xFFFFFFFFu - vid);
         atomicMax(&kbest[tok], key);

@@ -80,6 +80,8 @@ struct TmaSkinnyParams {
   int weights_once;            // MoE: each weight byte is read once per call (evict-first L2 policy)
   // ARGMAX (split 1): candidate j is weight row idx[j] (row j when idx is null)
   const int32_t* idx;
+  int64_t w_rows;              // rows gathered in place: rows of the weight; an idx entry outside
+                               // [0, w_rows) is skipped (compact rows: 0, idx holds labels only)
   unsigned long long* keys;    // [M] best (logit order key, ~id) so far, zero on entry
   unsigned int* counter;       // finished CTAs, zero on entry
   int32_t* out_ids;
@@ -258,6 +260,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
       const int64_t j0 = row_tile * GV_ROWS + 4 * lane + i;
       const int64_t j = j0 < p.n_rows ? j0 : p.n_rows - 1;
       rid[i] = p.idx ? p.idx[j] : static_cast<int>(j);
+      if (rid[i] < 0 || rid[i] >= p.w_rows) rid[i] = 0;   // a skipped entry reads row 0; its key is dropped
     }
     auto issue_weights = [&](int st) {
       const int q = st % C::STAGES;
@@ -451,7 +454,7 @@ __global__ void __launch_bounds__(GtWarps<MT, KW>::THREADS, 2)
         } else if (MODE == SK_ARGMAX) {
           // key: logit order first, then the lower vocabulary id
           const int64_t j = row_tile * GV_ROWS + r;
-          if (j < p.n_rows) {
+          if (j < p.n_rows && (!GATHERED || (sidx[r] >= 0 && sidx[r] < p.w_rows))) {
             const uint32_t vid = static_cast<uint32_t>(sidx[r]);
             key = (static_cast<unsigned long long>(float_order_key(v * mul)) << 32) | (0xFFFFFFFFu - vid);
           }
@@ -680,7 +683,8 @@ static __global__ void __launch_bounds__(RS_THREADS, 1)
       if (lane < RS_ROWS) {
         const int64_t j0 = group * RS_ROWS + lane;
         const int64_t j = j0 < p.n_rows ? j0 : p.n_rows - 1;
-        const int64_t v = p.idx ? static_cast<int64_t>(p.idx[j]) : j;
+        int64_t v = p.idx ? static_cast<int64_t>(p.idx[j]) : j;
+        if (v < 0 || v >= p.w_rows) v = 0;   // a skipped entry reads row 0; its key is dropped
         bulk_load(stage + lane * L.code_stride, p.codes + v * KB, static_cast<uint32_t>(KB), full_bar(q));
         bulk_load(stage + RS_ROWS * L.code_stride + lane * L.scale_stride, p.scales + v * KS,
                   static_cast<uint32_t>(KS), full_bar(q));
@@ -761,12 +765,13 @@ static __global__ void __launch_bounds__(RS_THREADS, 1)
       if (tid < RS_ROWS * 8) {
         const int r = tid >> 3, tok = tid & 7;
         const int64_t j = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) * RS_ROWS + r;
-        if (tok < M && j < p.n_rows) {
+        const int64_t vj = j < p.n_rows ? (p.idx ? static_cast<int64_t>(p.idx[j]) : j) : -1;
+        if (tok < M && vj >= 0 && vj < p.w_rows) {
           const float* rr = red + (i & 1) * (RS_CONSUMERS * RS_ROWS * 8) + r * 8 + tok;
           float v = 0.f;
 #pragma unroll
           for (int w = 0; w < RS_CONSUMERS; ++w) v += rr[w * RS_ROWS * 8];
-          const uint32_t vid = p.idx ? static_cast<uint32_t>(p.idx[j]) : static_cast<uint32_t>(j);
+          const uint32_t vid = static_cast<uint32_t>(vj);
           atomicMax(&kbest[tok], (static_cast<unsigned long long>(float_order_key(v * ldexpf(st, p.pexp[tok])))
                                   << 32) | (0xFFFFFFFFu - vid));
         }

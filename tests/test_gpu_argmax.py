@@ -40,6 +40,31 @@ def test_small_head(M, masked):
                          None if idx is None else idx.numpy())
 
 
+@pytest.mark.parametrize("M", [1, 4, 12, 32])
+@pytest.mark.parametrize("K", [512, 384])
+def test_index_entries_outside_the_weight_are_skipped(M, K):
+    """Rows gathered in place (M <= 8 whole-row streaming at K % 256 == 0,
+    tile::gather4 above, the register-fed kernel at K = 384): entries outside
+    [0, V) are never read nor reported, so the result equals the argmax over
+    the valid entries; with no valid entry the id is -1."""
+    m = nv()
+    V = 3000
+    w = synth.normal_f32((V, K), 0.02, seed=91)
+    idx = synth.permutation_prefix(V, 700, seed=92).clone()
+    bad = [3, 50, 400, 699]
+    for pos, val in zip(bad, (-1, V, V + 7, -(2 ** 31))):
+        idx[pos] = val
+    good = np.array([i for i in range(len(idx)) if i not in bad])
+    h = synth.normal_bf16((M, K), seed=93 + M)
+    qw = m.quantize(w.to(DEV))
+    ids, logit = m.gather_gemv_argmax(h.to(DEV), qw, idx.to(DEV))
+    check_against_oracle(ids.cpu().numpy(), logit.cpu().numpy(), h.float().numpy(), O.quantize(w.numpy()),
+                         idx.numpy()[good])
+    none = torch.tensor([-1, V, -5, V + 1], dtype=torch.int32)
+    ids0, logit0 = m.gather_gemv_argmax(h.to(DEV), qw, none.to(DEV))
+    assert (ids0.cpu() == -1).all() and torch.isnan(logit0.cpu()).all()
+
+
 def test_identity_index_equals_full_and_repeat_calls_agree():
     m = nv()
     V, K = 1000, 256
